@@ -1,0 +1,448 @@
+"""Benchmark of the fused inverse-RoPE + VHA postmix hot path on GB300.
+
+One step = one layer of the production shard: forward (Y), backward (dO, dM)
+and one KV index remap of the remap workload. The timed region runs K steps
+back to back with a fresh M per layer (37 layers cycled), inputs resident in
+HBM (1 GiB O / dY and a 512 MiB index table, each larger than the 129 MB L2, so
+no flush is needed between steps). Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the fp64 CPU oracle (the only reference this
+method has here) on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from partial_inverse_rope_gb300 import inputs as W  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["partial_inverse_rope_gb300/csrc/postmix.cu",
+                  "partial_inverse_rope_gb300/csrc/ptx.cuh"]
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "postmix_bwd_production_shard.md")
+
+
+# ---------------------------------------------------------------- environment
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """Per-launch DRAM bytes of the backward kernel from the committed ncu
+    summary, or None when the summary is missing or predates the current
+    kernel source."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    traffic = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not src or not traffic or src.group(1) != kernel_source_hash():
+        return None
+    return int(traffic.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) taken while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local):
+    import partial_inverse_rope_gb300 as ir
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    c = W.PROD
+    R = W.REMAP
+    # inputs resident in HBM (seeded, synthetic)
+    O, dY, _ = W.postmix_inputs(c, device=dev)
+    Ms = [W.postmix_M(c.nh, c.seed + 2 + l, dev) for l in range(c.layers)]
+    idx = W.kv_index_table(R, device=dev)
+    Y = torch.empty_like(O)
+    dO = torch.empty_like(O)
+    dM = torch.empty(c.nh, c.nh, dtype=torch.float32, device=dev)
+    ws = torch.empty(max(16, ir.invrope_postmix_bwd_workspace_bytes(c.sq, c.nh, c.nope, c.pe)),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty_like(idx)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(l, ev=None):
+        M = Ms[l % len(Ms)]
+        if ev is not None:
+            ev[0].record(stream)
+        ir.invrope_postmix_fwd(O, M, c.pos0, c.nope, c.pe, c.theta, Y=Y)
+        if ev is not None:
+            ev[1].record(stream)
+        ir.invrope_postmix_bwd(dY, O, M, c.pos0, c.nope, c.pe, c.theta, dO=dO, dM=dM, workspace=ws)
+        if ev is not None:
+            ev[2].record(stream)
+        ir.kv_idx_local_to_global(idx, R.sq, R.seqlen_kv, out=out)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for l in range(args.warmup):
+        step(l)
+    torch.cuda.synchronize()
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t0.record(stream)
+        for k in range(args.steps):
+            step(k, events[k])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms_total = t0.elapsed_time(t1)
+    fwd_us = [e[0].elapsed_time(e[1]) * 1e3 for e in events]
+    bwd_us = [e[1].elapsed_time(e[2]) * 1e3 for e in events]
+    remap_us = [e[2].elapsed_time(e[3]) * 1e3 for e in events]
+    ms_total = max_over_ranks(ms_total, world)
+    fault = ir.invrope_take_device_fault()
+
+    step_bytes = c.fwd_bytes() + c.bwd_bytes() + R.bytes()
+    ms_per_step = ms_total / args.steps
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9  # GB/s over all ranks
+
+    # end to end through the public API with host buffers: pinned host -> device
+    # inputs, the three calls, device -> pinned host outputs, all inside the timed region
+    e2e = run_e2e(args, ir, c, R, dev, stream, O, dY, Ms, idx, Y, dO, dM, ws, out, world)
+
+    peak, peak_kind = measured_peak()
+    bwd_avg = statistics.mean(bwd_us)
+    achieved = c.bwd_bytes() / (bwd_avg * 1e-6) / 1e9
+    line = {
+        "metric": "fused inv-RoPE+postmix fwd/bwd us and HBM GB/s (% of roof), sq=16384 nh=64",
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) bf16 O/dY, M = I + 0.02 N(0,1) fp32 per layer, "
+                "int32 uniform KV table with 5% -1 padding",
+        "config": {
+            "workload": "production shard fwd+bwd (sq=16384, nh=64, nope=448, pe=64, positions "
+                        "16384..32767, 37 layers cycled) + KV index remap (b=4, sq=16384, "
+                        "topk=2048, seqlen_kv=16384)",
+            "sq": c.sq, "nh": c.nh, "nope": c.nope, "pe": c.pe, "pos0": c.pos0,
+            "theta": c.theta, "layers": c.layers,
+            "remap": {"b": R.b, "sq": R.sq, "topk": R.topk, "seqlen_kv": R.seqlen_kv},
+            "parallelism": "replicas" if world > 1 else "single",
+            "l2": "inputs larger than L2 (1 GiB / 512 MiB per tensor), no flush",
+        },
+        "kernels_us": {
+            "fwd": round(statistics.mean(fwd_us), 2),
+            "bwd": round(bwd_avg, 2),
+            "remap": round(statistics.mean(remap_us), 2),
+        },
+        "kernels_gbs": {
+            "fwd": round(c.fwd_bytes() / (statistics.mean(fwd_us) * 1e-6) / 1e9, 1),
+            "bwd": round(achieved, 1),
+            "remap": round(R.bytes() / (statistics.mean(remap_us) * 1e-6) / 1e9, 1),
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "invrope_postmix_bwd (main kernel + dM reduce, per call)",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": peak_kind,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic(),
+            "algorithmic_bytes_per_launch": c.bwd_bytes(),
+        },
+        "e2e": e2e,
+        "gpu_launches": args.steps * 4,
+        "clocks": clocks.summary(),
+        "device_fault": fault,
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(args)
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, ir, c, R, dev, stream, O, dY, Ms, idx, Y, dO, dM, ws, out, world):
+    hO = torch.empty(O.shape, dtype=O.dtype, pin_memory=True)
+    hdY = torch.empty(dY.shape, dtype=dY.dtype, pin_memory=True)
+    hM = [torch.empty(m.shape, dtype=m.dtype, pin_memory=True) for m in Ms]
+    hidx = torch.empty(idx.shape, dtype=idx.dtype, pin_memory=True)
+    hO.copy_(O)
+    hdY.copy_(dY)
+    for h, m in zip(hM, Ms):
+        h.copy_(m)
+    hidx.copy_(idx)
+    hY = torch.empty_like(hO, pin_memory=True)
+    hdO = torch.empty_like(hdY, pin_memory=True)
+    hdM = torch.empty(c.nh, c.nh, dtype=torch.float32, pin_memory=True)
+    hout = torch.empty_like(hidx, pin_memory=True)
+    dM_dev = dM
+
+    def e2e_step(l):
+        O.copy_(hO, non_blocking=True)
+        dY.copy_(hdY, non_blocking=True)
+        M = Ms[l % len(Ms)]
+        M.copy_(hM[l % len(hM)], non_blocking=True)
+        idx.copy_(hidx, non_blocking=True)
+        ir.invrope_postmix_fwd(O, M, c.pos0, c.nope, c.pe, c.theta, Y=Y)
+        ir.invrope_postmix_bwd(dY, O, M, c.pos0, c.nope, c.pe, c.theta, dO=dO, dM=dM_dev, workspace=ws)
+        ir.kv_idx_local_to_global(idx, R.sq, R.seqlen_kv, out=out)
+        hY.copy_(Y, non_blocking=True)
+        hdO.copy_(dO, non_blocking=True)
+        hdM.copy_(dM_dev, non_blocking=True)
+        hout.copy_(out, non_blocking=True)
+
+    steps = max(1, min(args.steps, 5))
+    for l in range(min(2, args.warmup)):
+        e2e_step(l)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for l in range(steps):
+        e2e_step(l)
+    torch.cuda.synchronize()
+    dt = max_over_ranks((time.perf_counter() - t0) * 1e3, world) / steps
+    step_bytes = c.fwd_bytes() + c.bwd_bytes() + R.bytes()
+    h2d = hO.numel() * 2 + hdY.numel() * 2 + c.nh * c.nh * 4 + hidx.numel() * 4
+    d2h = hY.numel() * 2 + hdO.numel() * 2 + c.nh * c.nh * 4 + hout.numel() * 4
+    return {"value": round(world * step_bytes / (dt * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(dt, 3), "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- oracle (CPU) legs
+def oracle_sample(rows: int, threads_note=True):
+    """Time the fp64 oracle on the first `rows` positions of the production shard
+    (fwd + bwd incl. dM) plus a proportional slice of the remap table; returns
+    (seconds, algorithmic bytes covered)."""
+    import numpy as np
+
+    import oracle
+
+    c = W.PROD
+    R = W.REMAP
+    O, dY, M = W.postmix_inputs(W.PostmixConfig("sample", sq=rows, nh=c.nh, nope=c.nope, pe=c.pe,
+                                                pos0=c.pos0, seed=c.seed), device="cpu")
+    frac = rows / c.sq
+    remap_rows = max(R.sq, int(R.rows * frac) // R.sq * R.sq)
+    idx = W.kv_index_table(W.RemapConfig("sample", b=remap_rows // R.sq, sq=R.sq, topk=R.topk,
+                                         seqlen_kv=R.seqlen_kv), device="cpu")
+    O64 = O.to(torch.float64).numpy()
+    dY64 = dY.to(torch.float64).numpy()
+    M64 = M.to(torch.float64).numpy()
+    idx_np = idx.numpy()
+    pos = np.arange(c.pos0, c.pos0 + rows, dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.postmix_fwd(O64, M64, pos, c.nope, c.pe, c.theta)
+    oracle.postmix_bwd(dY64, O64, M64, pos, c.nope, c.pe, c.theta)
+    oracle.kv_idx_local_to_global(idx_np, R.sq, R.seqlen_kv)
+    dt = time.perf_counter() - t0
+    nbytes = (2 * rows * c.nh * c.d * 2 + 4 * c.nh * c.nh) + (3 * rows * c.nh * c.d * 2 + 8 * c.nh * c.nh) \
+        + 2 * idx.numel() * 4
+    return dt, nbytes, rows, idx.shape[0]
+
+
+def oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def cpu_baseline(args):
+    rows = int(os.environ.get("INVROPE_ORACLE_ROWS", "1024"))
+    dt, nbytes, rows, idx_rows = oracle_sample(rows)
+    return {"value": round(nbytes / dt / 1e9, 3), "unit": "GB/s", "cores": oracle_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 numpy oracle: fwd+bwd(dO, dM) on the first {rows} of 16384 positions "
+                      f"of the production shard + remap of {idx_rows} table rows; "
+                      f"{dt:.2f} s wall, scaled to algorithmic GB/s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    rows = int(os.environ.get("INVROPE_ORACLE_ROWS", "256"))
+    times = []
+    nbytes = 0
+    for _ in range(args.warmup):
+        oracle_sample(rows)
+    for _ in range(args.steps):
+        dt, nbytes, rows, idx_rows = oracle_sample(rows)
+        times.append(dt)
+    sec = statistics.mean(times)
+    value = nbytes / sec / 1e9
+    c = W.PROD
+    line = {
+        "impl": "reference",
+        "metric": "fused inv-RoPE+postmix fwd/bwd us and HBM GB/s (% of roof), sq=16384 nh=64",
+        "value": round(value, 3),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (same recipe as the GPU arm)",
+        "config": {"workload": "production shard fwd+bwd + KV index remap, bounded sample "
+                               f"({rows} of {c.sq} positions per step)",
+                   "sq": c.sq, "nh": c.nh, "nope": c.nope, "pe": c.pe, "pos0": c.pos0},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "kind": "oracle",
+                         "cores": oracle_threads(),
+                         "sample": f"{rows} positions per step + the proportional remap slice"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=37)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,167 @@
+/*
+ * invrope.h -- C ABI of the GB300 (sm_103a) inverse-RoPE + VHA postmix
+ * library and its sparse-attention KV index remap.
+ *
+ * The operations are those of PaddleFleet pull request #1772, "Fuse HCA
+ * inverse RoPE into the VHA postmix, and the sparse-attention KV index
+ * remap" (cited below as [PR1772]):
+ *
+ *   [PR1772] English description, item 1 (fuse_inv_rope_into_vha_postmix):
+ *     the HCA inverse RoPE rotates back only the trailing pe channels of each
+ *     head of the attention output, and the ungrouped VHA postmix is an
+ *     [nh, nh] GEMM over the head axis. The channel axis is therefore a pure
+ *     N dimension and no full-width inv_rope(O) is needed.
+ *   [PR1772] Chinese description, section 1: the weight gradient
+ *     dM[h, h'] = sum_{t,c} dOut[t,h,c] * O_roped[t,h',c] over all tokens and
+ *     the full channel axis.
+ *   [PR1772] revision note: the input gradient is the postmix GEMM's input
+ *     gradient pushed back through the rotation.
+ *   [PR1772] English item 2 / Chinese section 2
+ *     (sparse_attn_global_kv_idx_remap_fusion): per-batch-local -> flat-global
+ *     KV column remap idx + b * seqlen_kv over a [b*sq, topk] table.
+ *
+ * Notation (all tensors dense, row-major, last index fastest):
+ *   O, Y, dY, dO : bf16 [sq, nh, d], d = nope + pe, channel fastest.
+ *   M, dM        : fp32 [nh, nh], row-major; Y[s,g,:] = sum_h M[g,h] X[s,h,:].
+ *   positions    : row s sits at absolute position p = pos0 + s.
+ *   rotary pairs : rotate-half, pair i = (nope+i, nope+i+pe/2), i < pe/2,
+ *                  frequency f_i = theta^(-2i/pe), angle a = p * f_i.
+ *   invrope      : (x1, x2) -> (x1 cos a + x2 sin a, x2 cos a - x1 sin a).
+ *   rope         : (x1, x2) -> (x1 cos a - x2 sin a, x2 cos a + x1 sin a).
+ *
+ * Common contract of every call below:
+ *   - Pointers are DEVICE pointers of the current CUDA device, owned by the
+ *     caller. The library allocates no device memory and keeps no state
+ *     between calls beyond cached device attributes and loaded kernels.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Every call
+ *     only enqueues work on `stream` and returns; nothing synchronises.
+ *   - Arguments are validated on the host before anything is enqueued; a
+ *     rejected call enqueues nothing and returns a non-zero status.
+ *   - A launch failure returns INVROPE_ERR_CUDA (the CUDA error is left for
+ *     cudaGetLastError / invrope_last_cuda_error).
+ *   - Kernel waits are bounded: a wait that runs out (about two seconds)
+ *     records a fault code that invrope_take_device_fault() returns, and the
+ *     kernel exits early instead of hanging. Outputs are then undefined.
+ *   - The device must be compute capability 10.3 (GB300, sm_103a);
+ *     otherwise calls return INVROPE_ERR_DEVICE.
+ */
+#ifndef INVROPE_H_
+#define INVROPE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t == struct CUstream_st* */
+
+typedef enum invrope_status {
+  INVROPE_OK = 0,
+  INVROPE_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad size, overlap */
+  INVROPE_ERR_UNSUPPORTED = 2, /* valid shape outside what the kernels cover   */
+  INVROPE_ERR_WORKSPACE = 3,   /* workspace missing or too small               */
+  INVROPE_ERR_CUDA = 4,        /* a CUDA runtime / launch error                */
+  INVROPE_ERR_DEVICE = 5       /* current device is not sm_103 (GB300)         */
+} invrope_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* invrope_status_string(int status);
+
+/* The last CUDA error code seen by the library on this thread (0 = none). */
+int invrope_last_cuda_error(void);
+
+/*
+ * Forward of the fused inverse RoPE + ungrouped VHA postmix
+ * ([PR1772] English item 1, Chinese section 1):
+ *
+ *   Y[s, g, :] = sum_h M[g, h] * invrope_{pos0+s}(O[s, h, :])
+ *
+ * O  : bf16 [sq, nh, d], input, 16-byte aligned.
+ * M  : fp32 [nh, nh] row-major, input, 4-byte aligned.
+ * Y  : bf16 [sq, nh, d], output (fully overwritten), 16-byte aligned; must
+ *      not overlap O or M.
+ * sq : rows (>= 0; 0 enqueues nothing). sq * nh must be < 2^31.
+ * nh : heads, 1..128.
+ * nope, pe : leading unrotated / trailing rotated channels; pe even >= 2,
+ *      nope >= 0, d = nope + pe a multiple of 8. The pe channels must lie in
+ *      one 64-channel-aligned block (nope / 64 == (d - 1) / 64), which holds
+ *      for every DeepSeek-style split with pe <= 64 such as 448 + 64;
+ *      otherwise INVROPE_ERR_UNSUPPORTED.
+ * pos0 : absolute position of row 0 (>= 0); theta : rotary base (> 0, finite).
+ * The head mix runs on the tensor cores with M split into two bf16 terms
+ * (hi + lo) and fp32 accumulation; the rotation is applied to the fp32
+ * accumulator, and Y is rounded to nearest-even bf16 once.
+ */
+int invrope_postmix_fwd(const void* O, const float* M, void* Y,
+                        int64_t sq, int nh, int nope, int pe,
+                        int64_t pos0, double theta,
+                        struct CUstream_st* stream);
+
+/*
+ * Workspace bytes invrope_postmix_bwd needs on the CURRENT device for this
+ * shape (one fp32 [nh, nh] partial of dM per thread block, so it depends on
+ * the device's SM count). Returns 0 when the shape is invalid or unsupported.
+ */
+size_t invrope_postmix_bwd_workspace_bytes(int64_t sq, int nh, int nope, int pe);
+
+/*
+ * Backward of invrope_postmix_fwd ([PR1772] Chinese section 1 and revision
+ * note), in one pass over dY and O plus a small fixed-order reduction:
+ *
+ *   dO[s, h, :] = rope_{pos0+s}( sum_g M[g, h] * dY[s, g, :] )   (bf16)
+ *   dM[g, h]    = sum_{s, c} dY[s, g, c] * X[s, h, c],  X = invrope(O) (fp32)
+ *
+ * dY, O : bf16 [sq, nh, d] inputs, 16-byte aligned.
+ * M     : fp32 [nh, nh] input.
+ * dO    : bf16 [sq, nh, d] output (overwritten), 16-byte aligned.
+ * dM    : fp32 [nh, nh] output, OVERWRITTEN (not accumulated into).
+ * workspace / workspace_bytes : caller-owned device scratch of at least
+ *      invrope_postmix_bwd_workspace_bytes() bytes, 16-byte aligned; its
+ *      contents on entry do not matter and are clobbered.
+ * Outputs must not overlap each other, the inputs or the workspace.
+ * Other arguments as in invrope_postmix_fwd. sq = 0 writes dM = 0.
+ * dM is bitwise identical from run to run on the same device: partials are
+ * formed per thread block in a fixed order and summed in block order (fp64
+ * accumulation) without atomics. The rotated pe operand of dM is split into
+ * bf16 hi + lo terms so that dM is not limited by bf16 rounding of X.
+ */
+int invrope_postmix_bwd(const void* dY, const void* O, const float* M,
+                        void* dO, float* dM,
+                        void* workspace, size_t workspace_bytes,
+                        int64_t sq, int nh, int nope, int pe,
+                        int64_t pos0, double theta,
+                        struct CUstream_st* stream);
+
+/*
+ * Per-batch-local -> flat-global sparse-attention KV column remap
+ * ([PR1772] English item 2, Chinese section 2), one pass over the table:
+ *
+ *   out[r, k] = idx[r, k] < 0 ? idx[r, k] : idx[r, k] + (r / sq) * seqlen_kv
+ *
+ * idx : int32 [rows, topk] input, 4-byte aligned.
+ * out : int32 [rows, topk] output; may be idx itself (in place) but must not
+ *       otherwise overlap it.
+ * rows = b * sq (rows % sq == 0), topk >= 0, sq >= 1, seqlen_kv >= 0, and
+ * b * seqlen_kv <= 2^31 so that every in-range index (0 <= idx < seqlen_kv)
+ * maps into int32. Entries >= seqlen_kv are not clamped; the add wraps in
+ * 32-bit two's complement. Bit-exact; an empty table enqueues nothing.
+ */
+int kv_idx_local_to_global(const int32_t* idx, int32_t* out,
+                           int64_t rows, int topk, int64_t sq,
+                           int64_t seqlen_kv, struct CUstream_st* stream);
+
+/*
+ * Synchronises the current device, then returns in *fault the watchdog code
+ * recorded by any kernel of this library on this device since the previous
+ * call (0 = none) and clears it. A non-zero code means a bounded wait ran
+ * out and that launch's outputs are undefined.
+ */
+int invrope_take_device_fault(int* fault);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* INVROPE_H_ */

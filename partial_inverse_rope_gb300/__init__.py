@@ -1,0 +1,15 @@
+"""GB300-native fused inverse RoPE + VHA postmix (forward / backward) and the
+sparse-attention KV index remap, as hand-written sm_103a CUDA kernels behind a
+C ABI (``include/invrope.h``), with a thin ctypes binding of the same names.
+"""
+
+from .binding import (  # noqa: F401
+    InvropeError,
+    invrope_postmix_bwd,
+    invrope_postmix_bwd_workspace_bytes,
+    invrope_postmix_fwd,
+    invrope_take_device_fault,
+    kv_idx_local_to_global,
+    lib,
+    lib_path,
+)

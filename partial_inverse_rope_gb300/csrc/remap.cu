@@ -1,0 +1,109 @@
+// Per-batch-local -> flat-global sparse-attention KV column remap on GB300.
+//
+// PaddleFleet PR #1772, "Fuse HCA inverse RoPE into the VHA postmix, and the
+// sparse-attention KV index remap", English description item 2 and Chinese
+// description section 2: out = idx + b * seqlen_kv over the [b*sq, topk]
+// table, padding (negative entries) kept, in one pass instead of the eager
+// chain of seven elementwise kernels.
+//
+// The table is streamed once as a flat array. Batch b owns the contiguous
+// element range [b*sq*topk, (b+1)*sq*topk), so a thread block that walks a
+// chunk of the flat array finds its batch with one division per chunk and
+// at most one boundary inside it. 16-byte vectors when the layout allows.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "common.h"
+
+namespace invrope {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kPer = 8;                         // vectors per thread per chunk
+constexpr int kChunk = kThreads * kPer;         // vectors per chunk
+
+__device__ __forceinline__ int32_t remap1(int32_t v, uint32_t off) {
+  return v < 0 ? v : static_cast<int32_t>(static_cast<uint32_t>(v) + off);
+}
+
+__device__ __forceinline__ int4 load_vec(const int4* p) { return __ldcs(p); }
+__device__ __forceinline__ int load_vec(const int* p) { return __ldcs(p); }
+__device__ __forceinline__ void store_vec(int4* p, int4 v) { __stcs(p, v); }
+__device__ __forceinline__ void store_vec(int* p, int v) { __stcs(p, v); }
+
+__device__ __forceinline__ int4 remap_vec(int4 v, uint32_t off) {
+  v.x = remap1(v.x, off);
+  v.y = remap1(v.y, off);
+  v.z = remap1(v.z, off);
+  v.w = remap1(v.w, off);
+  return v;
+}
+__device__ __forceinline__ int remap_vec(int v, uint32_t off) { return remap1(v, off); }
+
+// V = int4 (4 entries) or int (1 entry). seg = entries of one batch in units of V.
+// kOneBoundary: seg >= kChunk, so a chunk crosses at most one batch boundary.
+template <typename V, bool kOneBoundary>
+__global__ void __launch_bounds__(kThreads) kv_remap_kernel(const V* in, V* out, int64_t n, int64_t seg,
+                                                            uint32_t seqlen_kv) {
+  const int64_t nchunks = (n + kChunk - 1) / kChunk;
+  for (int64_t ch = blockIdx.x; ch < nchunks; ch += gridDim.x) {
+    const int64_t v0 = ch * kChunk;
+    const int64_t b0 = v0 / seg;
+    const int64_t boundary = (b0 + 1) * seg;
+    V x[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int64_t v = v0 + k * kThreads + threadIdx.x;
+      if (v < n) x[k] = load_vec(in + v);
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int64_t v = v0 + k * kThreads + threadIdx.x;
+      if (v < n) {
+        const int64_t b = kOneBoundary ? b0 + (v >= boundary ? 1 : 0) : v / seg;
+        const uint32_t off = static_cast<uint32_t>(static_cast<uint64_t>(b) * seqlen_kv);
+        store_vec(out + v, remap_vec(x[k], off));
+      }
+    }
+  }
+}
+
+template <typename V>
+int launch(const void* in, void* out, int64_t n, int64_t seg, uint32_t skv, int sms, cudaStream_t s) {
+  const int64_t nchunks = (n + kChunk - 1) / kChunk;
+  const int64_t grid = nchunks < static_cast<int64_t>(sms) * 8 ? nchunks : static_cast<int64_t>(sms) * 8;
+  if (seg >= kChunk)
+    kv_remap_kernel<V, true><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(
+        static_cast<const V*>(in), static_cast<V*>(out), n, seg, skv);
+  else
+    kv_remap_kernel<V, false><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(
+        static_cast<const V*>(in), static_cast<V*>(out), n, seg, skv);
+  return check_launch();
+}
+
+}  // namespace
+}  // namespace invrope
+
+using namespace invrope;
+
+extern "C" int kv_idx_local_to_global(const int32_t* idx, int32_t* out, int64_t rows, int topk, int64_t sq,
+                                      int64_t seqlen_kv, struct CUstream_st* stream) {
+  if (rows < 0 || topk < 0 || sq < 1 || seqlen_kv < 0) return INVROPE_ERR_INVALID_ARG;
+  if (rows % sq != 0) return INVROPE_ERR_INVALID_ARG;
+  const int64_t nb = rows / sq;
+  if (nb > 0 && nb * seqlen_kv > (int64_t(1) << 31)) return INVROPE_ERR_INVALID_ARG;
+  const int64_t n = rows * static_cast<int64_t>(topk);
+  if (n == 0) return INVROPE_OK;
+  if (!idx || !out || !aligned(idx, 4) || !aligned(out, 4)) return INVROPE_ERR_INVALID_ARG;
+  if (idx != out && overlaps(idx, n * 4, out, n * 4)) return INVROPE_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  int st = current_device(&dev);
+  if (st != INVROPE_OK) return st;
+  const int64_t seg = sq * topk;  // entries per batch
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint32_t skv = static_cast<uint32_t>(seqlen_kv);
+  if (aligned(idx, 16) && aligned(out, 16) && seg % 4 == 0)
+    return launch<int4>(idx, out, n / 4, seg / 4, skv, dev.sms, s);
+  return launch<int>(idx, out, n, seg, skv, dev.sms, s);
+}
