@@ -135,6 +135,42 @@ int invrope_postmix_bwd(const void* dY, const void* O, const float* M,
                         struct CUstream_st* stream);
 
 /*
+ * Size of the fixed device scratch that invrope_postmix_bwd_noalloc uses in
+ * place of a workspace: 8 MiB, i.e. up to 512 dM partials at nh = 64.
+ */
+#define INVROPE_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * invrope_postmix_bwd without a workspace argument, for callers that may not
+ * allocate device memory on their call path (no cudaMalloc, no allocating
+ * library call) and have no scratch buffer to pass: e.g. a runtime whose
+ * device memory is all planned ahead, or a plugin interface that hands over
+ * only inputs and outputs. It is not an operation of the pages (no
+ * counterpart there); it computes exactly what invrope_postmix_bwd computes,
+ * with the same kernels, arguments (minus the workspace) and results.
+ *
+ * Scratch: a file-scope device array of INVROPE_NOALLOC_SCRATCH_BYTES that
+ * the library owns. Each device that loads the library's module keeps it until
+ * the process exits. The library allocates nothing at call time.
+ * Limit: shapes whose backward needs more than that
+ *   (invrope_postmix_bwd_workspace_bytes(sq, nh, nope, pe) > 8 MiB, e.g.
+ *   nh = 128 with 152 thread blocks) are refused with INVROPE_ERR_WORKSPACE;
+ *   use invrope_postmix_bwd for those.
+ * First call on a device: it looks up the array's device address with
+ *   cudaGetSymbolAddress (with that device current), which may load the
+ *   module; make this first call before any stream capture.
+ * Sharing: all calls on a device use the same array and leave their partials
+ *   in it. Nothing in it needs to start at zero (each call writes every
+ *   partial it reads), but calls whose work overlaps on the GPU (e.g. on two
+ *   streams at once) race on the array: order them.
+ */
+int invrope_postmix_bwd_noalloc(const void* dY, const void* O, const float* M,
+                                void* dO, float* dM,
+                                int64_t sq, int nh, int nope, int pe,
+                                int64_t pos0, double theta,
+                                struct CUstream_st* stream);
+
+/*
  * Per-batch-local -> flat-global sparse-attention KV column remap
  * ([PR1772] English item 2, Chinese section 2), one pass over the table:
  *

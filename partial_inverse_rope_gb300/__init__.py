@@ -6,6 +6,7 @@ C ABI (``include/invrope.h``), with a thin ctypes binding of the same names.
 from .binding import (  # noqa: F401
     InvropeError,
     invrope_postmix_bwd,
+    invrope_postmix_bwd_noalloc,
     invrope_postmix_bwd_workspace_bytes,
     invrope_postmix_fwd,
     invrope_take_device_fault,

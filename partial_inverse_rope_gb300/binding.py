@@ -40,6 +40,11 @@ _SIGNATURES = {
         ctypes.c_void_p, ctypes.c_size_t,
         ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_int64, ctypes.c_double, ctypes.c_void_p]),
+    "invrope_postmix_bwd_noalloc": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int64, ctypes.c_double, ctypes.c_void_p]),
     "kv_idx_local_to_global": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
         ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),
@@ -151,6 +156,29 @@ def invrope_postmix_bwd(dY, O, M, pos0: int, nope: int, pe: int, theta: float = 
                                    dM.data_ptr(), workspace.data_ptr(), ws_bytes, sq, nh, nope, pe,
                                    int(pos0), float(theta), _stream_handle(O.device, stream))
     _check(st, "invrope_postmix_bwd")
+    return dO, dM
+
+
+def invrope_postmix_bwd_noalloc(dY, O, M, pos0: int, nope: int, pe: int, dO, dM,
+                                theta: float = 10000.0, stream=None):
+    """Backward without a workspace, for callers that may not allocate device
+    memory on their call path: the library's own fixed scratch array
+    (``INVROPE_NOALLOC_SCRATCH_BYTES``) holds the dM partials. ``dO`` and
+    ``dM`` must be given (this wrapper allocates nothing either). Calls that
+    overlap on the GPU share that array and must be ordered."""
+    _need(dY, "dY", torch.bfloat16, 3)
+    _need(O, "O", torch.bfloat16, 3)
+    _need(M, "M", torch.float32, 2)
+    _need(dO, "dO", torch.bfloat16, 3)
+    _need(dM, "dM", torch.float32, 2)
+    sq, nh, d = O.shape
+    if dY.shape != O.shape or dO.shape != O.shape or tuple(M.shape) != (nh, nh) \
+            or tuple(dM.shape) != (nh, nh):
+        raise ValueError("dY/dO must match O; M and dM must be [nh, nh]")
+    st = lib().invrope_postmix_bwd_noalloc(dY.data_ptr(), O.data_ptr(), M.data_ptr(), dO.data_ptr(),
+                                           dM.data_ptr(), sq, nh, nope, pe, int(pos0), float(theta),
+                                           _stream_handle(O.device, stream))
+    _check(st, "invrope_postmix_bwd_noalloc")
     return dO, dM
 
 

@@ -22,7 +22,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libinvrope.so")
 
-SOURCES = ["postmix.cu", "remap.cu", "api.cpp"]
+SOURCES = ["postmix.cu", "remap.cu", "api.cpp", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
