@@ -31,8 +31,12 @@
  *
  * Common contract of every call below:
  *   - Pointers are DEVICE pointers of the current CUDA device, owned by the
- *     caller. The library allocates no device memory and keeps no state
- *     between calls beyond cached device attributes and loaded kernels.
+ *     caller. The library allocates no device memory at call time and keeps
+ *     no state between calls beyond cached device attributes, loaded kernels
+ *     and a 2 KB per-device array of tile counters: the forward hands out
+ *     its tiles dynamically (thread blocks claim the next tile from a
+ *     counter), and the last thread block of a launch returns its counter
+ *     to zero.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream). Every call
  *     only enqueues work on `stream` and returns; nothing synchronises.
  *   - Arguments are validated on the host before anything is enqueued; a

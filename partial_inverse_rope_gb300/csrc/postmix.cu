@@ -45,6 +45,12 @@ namespace invrope {
 
 __device__ unsigned int g_fault_code = 0;
 
+// Dynamic tile scheduling of the forward: one {next tile, finished CTAs} pair
+// per launch slot. A launch takes slot (launch sequence number mod
+// kSchedSlots); its last CTA returns the pair to zero.
+constexpr int kSchedSlots = 256;
+__device__ unsigned int g_sched[kSchedSlots][2];
+
 namespace {
 
 constexpr int kRowsMax = 128;                            // MMA M = rows of a tile
@@ -55,38 +61,45 @@ constexpr int kMaxHalf = 32;                             // pe / 2 <= 32
 constexpr uint64_t kWaitLimitNs = 2000000000ull;         // bounded waits: 2 s
 
 // fault codes: role in bits 8-11, barrier kind in bits 0-7
-enum : unsigned { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleTransform = 4 };
+enum : unsigned { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleTransform = 4, kRoleStore = 5 };
 enum : unsigned { kBarFull = 1, kBarEmpty, kBarAccFull, kBarAccEmpty, kBarXFull, kBarXEmpty,
-                  kBarD2, kBarDone, kBarXGo };
+                  kBarD2, kBarDone, kBarXGo, kBarOut };
 
 template <bool BWD>
 struct KCfg {
   static constexpr int NC = BWD ? 64 : 128;              // channels per tile
   static constexpr int kChunks = NC / kChunkCols;
-  static constexpr int kStages = 4;
   static constexpr int kTensorTile = kChunks * kChunkBytes;
-  static constexpr int kStageBytes = (BWD ? 2 : 1) * kTensorTile;
-  static constexpr int kNumAcc = 4;
-  static constexpr int kD2Col = kNumAcc * NC;            // dM accumulator column (bwd)
+  static constexpr int kStageBytes = (BWD ? 2 : 1) * kTensorTile;   // input ring entry
+  static constexpr int kStages = 4;                      // input ring
+  static constexpr int kOutBufs = BWD ? 4 : 5;           // output ring of 64-channel chunks
+  static constexpr int kOutInflight = kOutBufs - 2;      // TMA stores left reading smem
+  static constexpr int kNumAcc = BWD ? 4 : 3;
+  // TMEM columns: accumulators, then dM (bwd), then A hi (64) and A lo (64)
+  static constexpr int kD2Col = kNumAcc * NC;
+  static constexpr int kACol = 384;
   static constexpr int kTmemCols = 512;
-  static constexpr int kThreads = BWD ? 320 : 192;
+  // warps: 0 TMA producer, 1 MMA issuer, 2-5 epilogue, (6-9 transform,) last = TMA store
+  static constexpr int kWarpStore = BWD ? 10 : 6;
+  static constexpr int kThreads = (kWarpStore + 1) * 32;
   // shared-memory carve-up (bytes from the 1024-aligned base)
-  static constexpr int kOffA = 0;                        // A hi: 2 K-blocks, then A lo
-  static constexpr int kABytes = 4 * kChunkBytes;
-  static constexpr int kOffStage = kOffA + kABytes;
-  static constexpr int kOffXlo = kOffStage + kStages * kStageBytes;
+  static constexpr int kOffStage = 0;
+  static constexpr int kOffOut = kOffStage + kStages * kStageBytes;
+  static constexpr int kOffXlo = kOffOut + kOutBufs * kChunkBytes;
   static constexpr int kXloBytes = BWD ? kChunkBytes : 0;
   static constexpr int kTabBytes = kPosPerTileMax * kMaxHalf * 8;
   static constexpr int kOffTabEpi = kOffXlo + kXloBytes;
   static constexpr int kOffTabXf = kOffTabEpi + kTabBytes;
   static constexpr int kOffFreq = kOffTabXf + (BWD ? kTabBytes : 0);
   static constexpr int kOffBars = kOffFreq + kMaxHalf * 8;
-  static constexpr int kNumBars = 2 * kStages + 2 * kNumAcc + 5;
+  static constexpr int kNumBars = 2 * kStages + 2 * kOutBufs + 2 * kNumAcc + 5;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 32;  // tmem base, abort flag, 5 wait slots
+  static constexpr int kSmemBytes = kOffMisc + 192;      // tmem base, abort flag, wait slots, tile ids
   static constexpr int kSmemAlloc = kSmemBytes + 1024;   // slack to align the base
   static_assert(kSmemAlloc <= 232448, "shared memory budget");
-  static_assert(BWD ? (kD2Col + 128 <= kTmemCols) : (kNumAcc * NC <= kTmemCols), "TMEM budget");
+  static_assert(kNumAcc * NC + (BWD ? 128 : 0) <= kACol, "TMEM budget");
+  static_assert(kStages * kStageBytes >= 128 * 128 * 4, "dM partial reduction reuses the input ring");
+  static_assert(kOutInflight >= 1, "at least one store in flight");
 };
 
 struct PostmixParams {
@@ -95,6 +108,7 @@ struct PostmixParams {
   CUtensorMap tm_out;  // fwd: Y      bwd: dO
   const float* M;
   float* ws;           // bwd: per-CTA dM partials [gridDim.x][nh][nh]
+  unsigned int* sched; // fwd: this launch's {next tile, finished CTAs} counters
   int64_t sq;
   int64_t pos0;
   int64_t n_tiles;
@@ -204,6 +218,17 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
+// A_blk(i, j): blockdiag_P(M) (forward) or blockdiag_P(M^T) (backward), zero
+// outside the R x R block diagonal.
+template <bool BWD>
+__device__ __forceinline__ float a_blk(const PostmixParams& p, int i, int j) {
+  if (i < p.R && j < p.R && (i / p.nh) == (j / p.nh)) {
+    const int gi = i % p.nh, gj = j % p.nh;
+    return BWD ? __ldg(p.M + gj * p.nh + gi) : __ldg(p.M + gi * p.nh + gj);
+  }
+  return 0.f;
+}
+
 template <bool BWD>
 __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
     postmix_kernel(const __grid_constant__ PostmixParams p) {
@@ -216,25 +241,36 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   constexpr int S = C::kStages;
+  constexpr int OB = C::kOutBufs;
   constexpr int NA = C::kNumAcc;
 
   auto bar_full = [&](int s) { return base + C::kOffBars + 8u * s; };
   auto bar_empty = [&](int s) { return base + C::kOffBars + 8u * (S + s); };
-  auto bar_acc_full = [&](int a) { return base + C::kOffBars + 8u * (2 * S + a); };
-  auto bar_acc_empty = [&](int a) { return base + C::kOffBars + 8u * (2 * S + NA + a); };
-  const uint32_t bar_x_full = base + C::kOffBars + 8u * (2 * S + 2 * NA);
+  auto bar_ob_full = [&](int b) { return base + C::kOffBars + 8u * (2 * S + b); };
+  auto bar_ob_empty = [&](int b) { return base + C::kOffBars + 8u * (2 * S + OB + b); };
+  auto bar_acc_full = [&](int a) { return base + C::kOffBars + 8u * (2 * S + 2 * OB + a); };
+  auto bar_acc_empty = [&](int a) { return base + C::kOffBars + 8u * (2 * S + 2 * OB + NA + a); };
+  const uint32_t bar_x_full = base + C::kOffBars + 8u * (2 * S + 2 * OB + 2 * NA);
   const uint32_t bar_x_empty = bar_x_full + 8;
   const uint32_t bar_d2 = bar_x_full + 16;
   const uint32_t bar_done = bar_x_full + 24;
   const uint32_t bar_x_go = bar_x_full + 32;
   auto stage_addr = [&](int s) { return base + C::kOffStage + static_cast<uint32_t>(s) * C::kStageBytes; };
+  auto out_addr = [&](int b) { return base + C::kOffOut + static_cast<uint32_t>(b) * kChunkBytes; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 4);
-  volatile int* slot_epi = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 8);
-  volatile int* slot_d2 = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 12);
-  volatile int* slot_xf_full = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 16);
-  volatile int* slot_xf_empty = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 20);
-  volatile int* slot_xf_go = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 24);
+  volatile int* slot_epi = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 8);   // [2]
+  volatile int* slot_ob = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 16);   // [2]
+  volatile int* slot_d2 = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 24);
+  volatile int* slot_xf_full = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 28);
+  volatile int* slot_xf_empty = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 32);
+  volatile int* slot_xf_go = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 36);
+  // forward: tile ids handed from role to role (-1 = no more tiles)
+  volatile int* stage_tile = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 64);  // [S]
+  volatile int* acc_tile = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 96);    // [NA]
+  volatile int* ob_tile = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 128);    // [OB]
+  volatile int* ob_chunk = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 160);   // [OB]
+  static_assert(S <= 8 && NA <= 8 && OB <= 8, "tile-id slots");
   uint64_t* F = reinterpret_cast<uint64_t*>(gbase + C::kOffFreq);
   const int half = p.pe >> 1;
 
@@ -244,8 +280,12 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
       ptx::mbar_init(bar_full(s), 1);
       ptx::mbar_init(bar_empty(s), 1);
     }
+    for (int b = 0; b < OB; ++b) {
+      ptx::mbar_init(bar_ob_full(b), 128);
+      ptx::mbar_init(bar_ob_empty(b), 1);
+    }
     for (int a = 0; a < NA; ++a) {
-      ptx::mbar_init(bar_acc_full(a), 1);
+      ptx::mbar_init(bar_acc_full(a), BWD ? 1 : 2);
       ptx::mbar_init(bar_acc_empty(a), 128);
     }
     ptx::mbar_init(bar_x_full, 128);
@@ -265,39 +305,12 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
     ptx::tmem_alloc(base + C::kOffMisc, C::kTmemCols);
     ptx::tmem_relinquish();
   }
-
-  // A = blockdiag_P(M) (forward) or blockdiag_P(M^T) (backward), bf16 hi + lo,
-  // K-major with 128-byte swizzle: element (i, j) of K-block j/64 sits in row i.
-  for (int u = threadIdx.x; u < kRowsMax * 16; u += blockDim.x) {
-    const int i = u >> 4;
-    const int j0 = (u & 15) << 3;
-    uint32_t hw[4], lw[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float v[2];
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int j = j0 + 2 * q + t;
-        float x = 0.f;
-        if (i < p.R && j < p.R && (i / p.nh) == (j / p.nh)) {
-          const int gi = i % p.nh, gj = j % p.nh;
-          x = BWD ? __ldg(p.M + gj * p.nh + gi) : __ldg(p.M + gi * p.nh + gj);
-        }
-        v[t] = x;
-      }
-      hw[q] = ptx::pack_bf16x2(v[0], v[1]);
-      lw[q] = ptx::pack_bf16x2(v[0] - ptx::bf16_lo_f32(hw[q]), v[1] - ptx::bf16_hi_f32(hw[q]));
-    }
-    const int kb = j0 >> 6;
-    const int unit = (j0 & 63) >> 3;
-    const uint32_t off = kb * kChunkBytes + i * 128 + ((unit ^ (i & 7)) << 4);
-    ptx::st_shared_v4(base + C::kOffA + off, hw[0], hw[1], hw[2], hw[3]);
-    ptx::st_shared_v4(base + C::kOffA + 2 * kChunkBytes + off, lw[0], lw[1], lw[2], lw[3]);
-  }
-  // Zero every stage (rows >= R are never loaded and must read as 0) and X_lo.
-  for (uint32_t o = threadIdx.x * 16u; o < static_cast<uint32_t>(S * C::kStageBytes + C::kXloBytes);
-       o += blockDim.x * 16u)
+  // Zero the input ring (rows >= R are never loaded and must read as 0) and X_lo.
+  for (uint32_t o = threadIdx.x * 16u; o < static_cast<uint32_t>(S * C::kStageBytes); o += blockDim.x * 16u)
     ptx::st_shared_v4(base + C::kOffStage + o, 0u, 0u, 0u, 0u);
+  if (BWD)
+    for (uint32_t o = threadIdx.x * 16u; o < static_cast<uint32_t>(kChunkBytes); o += blockDim.x * 16u)
+      ptx::st_shared_v4(base + C::kOffXlo + o, 0u, 0u, 0u, 0u);
   if (threadIdx.x < half) {
     const double f = pow(p.theta, -2.0 * static_cast<double>(threadIdx.x) / p.pe);
     F[threadIdx.x] = __double2ull_rn(f * 0.15915494309189535 * 18446744073709551616.0);
@@ -308,6 +321,30 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  if (warp >= 2 && warp < 6) {
+    // A in TMEM: lane m holds row m; column kACol + hl*64 + j/2 holds the bf16
+    // pair (j, j+1) of the hi (hl = 0) or lo (hl = 1) term, lower j in the low half.
+    const uint32_t quad = static_cast<uint32_t>(warp & 3);
+    const int m = static_cast<int>(quad * 32) + lane;
+    const uint32_t row_addr = tmem_base + ((quad * 32u) << 16) + C::kACol;
+    for (int hl = 0; hl < 2; ++hl)
+      for (int kh = 0; kh < 2; ++kh) {
+        uint32_t w[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          const int j = kh * 64 + 2 * q;
+          const float v0 = a_blk<BWD>(p, m, j), v1 = a_blk<BWD>(p, m, j + 1);
+          const uint32_t h = ptx::pack_bf16x2(v0, v1);
+          w[q] = hl == 0 ? h : ptx::pack_bf16x2(v0 - ptx::bf16_lo_f32(h), v1 - ptx::bf16_hi_f32(h));
+        }
+        ptx::tmem_st_x32(row_addr + hl * 64 + kh * 32, w);
+      }
+    ptx::tmem_st_wait();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+
   const int64_t G = gridDim.x;
   const int64_t t_begin = p.n_tiles * blockIdx.x / G;
   const int64_t t_end = p.n_tiles * (blockIdx.x + 1) / G;
@@ -315,11 +352,25 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
-      int64_t i = 0;
-      for (int64_t t = t_begin; t < t_end; ++t, ++i) {
+      // forward: tiles are claimed from the launch's counter, one claim ahead
+      int64_t t_next = BWD ? t_begin : static_cast<int64_t>(atomicAdd(p.sched, 1u));
+      for (int64_t i = 0;; ++i) {
         const int st = static_cast<int>(i % S);
         const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
+        if (BWD && t_next >= t_end) break;
         if (!wait_bar(bar_empty(st), ph ^ 1u, abort_flag, (kRoleProducer << 8) | kBarEmpty)) break;
+        const int64_t t = t_next;
+        if (BWD) {
+          t_next = t + 1;
+        } else {
+          if (t >= p.n_tiles) {
+            stage_tile[st] = -1;  // published by the arrive below
+            ptx::mbar_arrive(bar_full(st));
+            break;
+          }
+          t_next = static_cast<int64_t>(atomicAdd(p.sched, 1u));
+          stage_tile[st] = static_cast<int>(t);
+        }
         const Tile x = decode_tile<BWD>(p, t);
         const uint32_t bytes = static_cast<uint32_t>(x.nch * p.R * 128 * (BWD ? 2 : 1));
         ptx::mbar_arrive_expect_tx(bar_full(st), bytes);
@@ -338,13 +389,22 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
       const uint32_t nks = static_cast<uint32_t>((p.R + 15) / 16);
       uint32_t d2_started = 0;
       int npe = 0;
-      int64_t i = 0;
-      for (int64_t t = t_begin; t < t_end; ++t, ++i) {
+      for (int64_t i = 0;; ++i) {
         const int st = static_cast<int>(i % S);
         const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
         const int acc = static_cast<int>(i % NA);
         const uint32_t aph = static_cast<uint32_t>((i / NA) & 1);
+        if (BWD && t_begin + i >= t_end) break;
         if (!wait_bar(bar_full(st), ph, abort_flag, (kRoleMma << 8) | kBarFull)) break;
+        const int64_t t = BWD ? t_begin + i : static_cast<int64_t>(stage_tile[st]);
+        if (!BWD && t < 0) {
+          // pass the end of the tile stream on to the epilogue
+          if (!wait_bar(bar_acc_empty(acc), aph ^ 1u, abort_flag, (kRoleMma << 8) | kBarAccEmpty)) break;
+          acc_tile[acc] = -1;
+          ptx::mbar_arrive(bar_acc_full(acc));
+          ptx::tc_commit(bar_acc_full(acc));
+          break;
+        }
         const Tile x = decode_tile<BWD>(p, t);
         // The transform warps only see pe tiles; this thread has observed every
         // stage phase in order, so it tells them when the pe tile has landed.
@@ -352,15 +412,13 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
         if (!wait_bar(bar_acc_empty(acc), aph ^ 1u, abort_flag, (kRoleMma << 8) | kBarAccEmpty)) break;
         ptx::tc_fence_after();
         const uint32_t sa = stage_addr(st);
-        // head mix: D[acc] = A_hi * B + A_lo * B, B = the tile (MN-major, K = rows)
+        // head mix: D[acc] = A_hi * B + A_lo * B, A in TMEM, B = the tile (MN-major, K = rows)
         const uint32_t d_acc = tmem_base + static_cast<uint32_t>(acc * C::NC);
         const uint32_t idesc_mix = ptx::idesc_bf16_f32(128, 64u * x.nch, false, true);
         for (uint32_t hl = 0; hl < 2; ++hl)
           for (uint32_t ks = 0; ks < nks; ++ks) {
-            const uint64_t ad = ptx::smem_desc_sw128(
-                base + C::kOffA + hl * 2 * kChunkBytes + (ks >> 2) * kChunkBytes + (ks & 3) * 32, 16, 1024);
             const uint64_t bd = ptx::smem_desc_sw128(sa + ks * 2048, kChunkBytes, 1024);
-            ptx::tc_mma_ss(d_acc, ad, bd, idesc_mix, (hl | ks) != 0);
+            ptx::tc_mma_ts(d_acc, tmem_base + C::kACol + hl * 64 + ks * 8, bd, idesc_mix, (hl | ks) != 0);
           }
         if (BWD && x.has_pe) {
           if (!wait_bar(bar_x_full, static_cast<uint32_t>(npe & 1), abort_flag, (kRoleMma << 8) | kBarXFull))
@@ -388,7 +446,10 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
             }
           }
         }
+        if (!BWD) acc_tile[acc] = static_cast<int>(t);
         ptx::tc_commit(bar_acc_full(acc));
+        if (!BWD) ptx::mbar_arrive(bar_acc_full(acc));  // publishes acc_tile[acc]
+        ptx::tc_commit(bar_empty(st));  // the input stage is free once these MMAs are done
         if (BWD && x.has_pe) {
           ptx::tc_commit(bar_x_empty);
           ++npe;
@@ -409,105 +470,152 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
     const int pl = row_ok ? r / p.nh : 0;
     float2* tab = reinterpret_cast<float2*>(gbase + C::kOffTabEpi);
     const float sgn = BWD ? 1.f : -1.f;  // rope (+a) for dO, inverse rope (-a) for Y
-    int st_prev = -1;
-    int64_t i = 0;
-    for (int64_t t = t_begin; t < t_end; ++t, ++i) {
-      const int st = static_cast<int>(i % S);
+    int64_t n = 0;  // output chunk counter (output ring position)
+    bool ok = true;
+    for (int64_t i = 0; ok; ++i) {
+      if (BWD && t_begin + i >= t_end) break;
       const int acc = static_cast<int>(i % NA);
       const uint32_t aph = static_cast<uint32_t>((i / NA) & 1);
       if (!group_wait(bar_acc_full(acc), aph, abort_flag, (kRoleEpilogue << 8) | kBarAccFull, e == 0,
-                      slot_epi, 1))
+                      slot_epi + (i & 1), 1))
         break;
       ptx::tc_fence_after();
+      const int64_t t = BWD ? t_begin + i : static_cast<int64_t>(acc_tile[acc]);
+      if (!BWD && t < 0) {
+        // pass the end of the tile stream on to the store warp
+        const int b = static_cast<int>(n % OB);
+        if (group_wait(bar_ob_empty(b), static_cast<uint32_t>(((n / OB) & 1) ^ 1), abort_flag,
+                       (kRoleEpilogue << 8) | kBarOut, e == 0, slot_ob + (n & 1), 1)) {
+          if (e == 0) ob_tile[b] = -1;
+          ptx::mbar_arrive(bar_ob_full(b));
+        }
+        break;
+      }
       const Tile x = decode_tile<BWD>(p, t);
+      const int pcol = p.nope - x.c0;  // tile-relative column of the first pe channel
       if (x.has_pe) {
         fill_rot_table(tab, F, p.pos0 + x.s0, p.P, half, e, 128);
         ptx::named_bar_sync(1, 128);
       }
-      const uint32_t out_tile = stage_addr(st);
       const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * C::NC);
-      for (int j0 = 0; j0 < x.nch * kChunkCols; j0 += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld_x32(taddr + j0, v);
-        ptx::tmem_ld_wait(v);
-        if (row_ok) {
+      for (int k = 0; k < x.nch; ++k, ++n) {
+        const int b = static_cast<int>(n % OB);
+        if (!group_wait(bar_ob_empty(b), static_cast<uint32_t>(((n / OB) & 1) ^ 1), abort_flag,
+                        (kRoleEpilogue << 8) | kBarOut, e == 0, slot_ob + (n & 1), 1)) {
+          ok = false;
+          break;
+        }
+        const uint32_t ob = out_addr(b);
+        const bool pe_chunk = x.has_pe && (pcol >> 6) == k;
+        const bool pe_whole = pe_chunk && half == 32;  // the pe block is exactly this chunk
+        if (!pe_whole) {
+          // one 64-column TMEM load, one wait, then 8 swizzled 16-byte stores
+          uint32_t v[64];
+          ptx::tmem_ld_x64(taddr + k * kChunkCols, v);
+          ptx::tmem_ld_wait(v);
+          if (row_ok) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint32_t w0 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]));
-            const uint32_t w1 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]));
-            const uint32_t w2 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]));
-            const uint32_t w3 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7]));
-            ptx::st_shared_v4(swz_unit_addr(out_tile, r, j0 + 8 * u), w0, w1, w2, w3);
+            for (int u = 0; u < 8; ++u) {
+              const uint32_t w0 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]));
+              const uint32_t w1 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]));
+              const uint32_t w2 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]));
+              const uint32_t w3 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7]));
+              ptx::st_shared_v4(swz_unit_addr(ob, r, 8 * u), w0, w1, w2, w3);
+            }
           }
         }
-      }
-      if (x.has_pe) {
-        // rotate the pe pairs of the fp32 accumulator, then round once
-        const int pcol = p.nope - x.c0;
-        const float2* rt = tab + pl * half;
-        if ((half & 7) == 0) {
-          for (int i0 = 0; i0 < half; i0 += 8) {
-            uint32_t a[8], b[8];
-            ptx::tmem_ld_x8(taddr + pcol + i0, a);
-            ptx::tmem_ld_x8(taddr + pcol + half + i0, b);
-            ptx::tmem_ld_wait(a, b);
-            if (row_ok) {
+        if (pe_whole) {
+          // pe = 64 filling the chunk: one load brings both halves of every pair
+          const float2* rt = tab + pl * 32;
+          uint32_t v[64];
+          ptx::tmem_ld_x64(taddr + pcol, v);
+          ptx::tmem_ld_wait(v);
+          if (row_ok) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
               uint32_t w1[4], w2[4];
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
                 float y1[2], y2[2];
 #pragma unroll
                 for (int s2 = 0; s2 < 2; ++s2) {
-                  const int k = 2 * q + s2;
-                  const float2 cs = rt[i0 + k];
-                  const float x1 = __uint_as_float(a[k]), x2 = __uint_as_float(b[k]);
+                  const int kq = 8 * u + 2 * q + s2;
+                  const float2 cs = rt[kq];
+                  const float x1 = __uint_as_float(v[kq]), x2 = __uint_as_float(v[32 + kq]);
                   y1[s2] = x1 * cs.x - sgn * x2 * cs.y;
                   y2[s2] = x2 * cs.x + sgn * x1 * cs.y;
                 }
                 w1[q] = ptx::pack_bf16x2(y1[0], y1[1]);
                 w2[q] = ptx::pack_bf16x2(y2[0], y2[1]);
               }
-              ptx::st_shared_v4(swz_unit_addr(out_tile, r, pcol + i0), w1[0], w1[1], w1[2], w1[3]);
-              ptx::st_shared_v4(swz_unit_addr(out_tile, r, pcol + half + i0), w2[0], w2[1], w2[2], w2[3]);
+              ptx::st_shared_v4(swz_unit_addr(ob, r, 8 * u), w1[0], w1[1], w1[2], w1[3]);
+              ptx::st_shared_v4(swz_unit_addr(ob, r, 32 + 8 * u), w2[0], w2[1], w2[2], w2[3]);
             }
           }
-        } else {
-          for (int ii = 0; ii < half; ++ii) {
-            uint32_t a, b;
-            ptx::tmem_ld_x1(taddr + pcol + ii, a);
-            ptx::tmem_ld_x1(taddr + pcol + half + ii, b);
-            ptx::tmem_ld_wait(a, b);
-            if (row_ok) {
-              const float2 cs = rt[ii];
-              const float x1 = __uint_as_float(a), x2 = __uint_as_float(b);
-              const int c1 = pcol + ii, c2 = pcol + half + ii;
-              st_shared_b16(swz_unit_addr(out_tile, r, c1) + (c1 & 7) * 2, bf16_bits(x1 * cs.x - sgn * x2 * cs.y));
-              st_shared_b16(swz_unit_addr(out_tile, r, c2) + (c2 & 7) * 2, bf16_bits(x2 * cs.x + sgn * x1 * cs.y));
+        } else if (pe_chunk) {
+          // rotate the pe pairs of the fp32 accumulator, then round once
+          const int qcol = pcol - k * kChunkCols;  // chunk-relative
+          const float2* rt = tab + pl * half;
+          if ((half & 7) == 0) {
+            for (int i0 = 0; i0 < half; i0 += 8) {
+              uint32_t a[8], bb[8];
+              ptx::tmem_ld_x8(taddr + pcol + i0, a);
+              ptx::tmem_ld_x8(taddr + pcol + half + i0, bb);
+              ptx::tmem_ld_wait(a, bb);
+              if (row_ok) {
+                uint32_t w1[4], w2[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  float y1[2], y2[2];
+#pragma unroll
+                  for (int s2 = 0; s2 < 2; ++s2) {
+                    const int kq = 2 * q + s2;
+                    const float2 cs = rt[i0 + kq];
+                    const float x1 = __uint_as_float(a[kq]), x2 = __uint_as_float(bb[kq]);
+                    y1[s2] = x1 * cs.x - sgn * x2 * cs.y;
+                    y2[s2] = x2 * cs.x + sgn * x1 * cs.y;
+                  }
+                  w1[q] = ptx::pack_bf16x2(y1[0], y1[1]);
+                  w2[q] = ptx::pack_bf16x2(y2[0], y2[1]);
+                }
+                ptx::st_shared_v4(swz_unit_addr(ob, r, qcol + i0), w1[0], w1[1], w1[2], w1[3]);
+                ptx::st_shared_v4(swz_unit_addr(ob, r, qcol + half + i0), w2[0], w2[1], w2[2], w2[3]);
+              }
+            }
+          } else {
+            for (int ii = 0; ii < half; ++ii) {
+              uint32_t a, bb;
+              ptx::tmem_ld_x1(taddr + pcol + ii, a);
+              ptx::tmem_ld_x1(taddr + pcol + half + ii, bb);
+              ptx::tmem_ld_wait(a, bb);
+              if (row_ok) {
+                const float2 cs = rt[ii];
+                const float x1 = __uint_as_float(a), x2 = __uint_as_float(bb);
+                const int c1 = qcol + ii, c2 = qcol + half + ii;
+                st_shared_b16(swz_unit_addr(ob, r, c1) + (c1 & 7) * 2, bf16_bits(x1 * cs.x - sgn * x2 * cs.y));
+                st_shared_b16(swz_unit_addr(ob, r, c2) + (c2 & 7) * 2, bf16_bits(x2 * cs.x + sgn * x1 * cs.y));
+              }
             }
           }
         }
+        // hand the finished 64-channel chunk to the store warp
+        if (!BWD && e == 0) {
+          ob_tile[b] = static_cast<int>(t);
+          ob_chunk[b] = k;
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(bar_ob_full(b));
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar_acc_empty(acc));
-      ptx::fence_proxy_async_smem();
-      ptx::named_bar_sync(1, 128);
-      if (e == 0) {
-        for (int k = 0; k < x.nch; ++k)
-          ptx::tma_store_2d(&p.tm_out, out_tile + k * kChunkBytes, x.c0 + k * kChunkCols, x.row0);
-        ptx::bulk_commit();
-        if (st_prev >= 0) {
-          ptx::bulk_wait_read<1>();
-          ptx::mbar_arrive(bar_empty(st_prev));
-        }
-        st_prev = st;
-      }
     }
-    if (e == 0) ptx::bulk_wait<0>();
-    if (BWD) {
-      // this CTA's dM share: sum of the diagonal nh x nh blocks of D2
+    if (BWD && ok) {
+      // This CTA's dM share: the sum of the diagonal nh x nh blocks of D2. The
+      // input ring is free once every MMA has completed.
       if (group_wait(bar_d2, 0, abort_flag, (kRoleEpilogue << 8) | kBarD2, e == 0, slot_d2, 1)) {
         ptx::tc_fence_after();
-        float* red = reinterpret_cast<float*>(gbase + C::kOffA);  // A is dead now
+        // red[h * R + r] = D2[r][pl*nh + h]: consecutive rows -> consecutive words
+        float* red = reinterpret_cast<float*>(gbase + C::kOffStage);
         const int lo = pl * p.nh;
         for (int j0 = 0; j0 < 128; j0 += 32) {
           uint32_t v[32];
@@ -517,19 +625,54 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
               const int j = j0 + jj;
-              if (j >= lo && j < lo + p.nh) red[r * p.nh + (j - lo)] = __uint_as_float(v[jj]);
+              if (j >= lo && j < lo + p.nh) red[(j - lo) * p.R + r] = __uint_as_float(v[jj]);
             }
           }
         }
         ptx::named_bar_sync(1, 128);
         const int nn = p.nh * p.nh;
         for (int idx = e; idx < nn; idx += 128) {
-          const int g = idx / p.nh, h = idx - g * p.nh;
+          const int h = idx / p.nh, g = idx - h * p.nh;
           float s = 0.f;
-          for (int q = 0; q < p.P; ++q) s += red[(q * p.nh + g) * p.nh + h];
-          p.ws[static_cast<int64_t>(blockIdx.x) * nn + idx] = s;
+          for (int q = 0; q < p.P; ++q) s += red[h * p.R + q * p.nh + g];
+          p.ws[static_cast<int64_t>(blockIdx.x) * nn + g * p.nh + h] = s;
         }
       }
+    }
+  } else if (warp == C::kWarpStore) {
+    // ---------------------------------------------------------- TMA store (output ring)
+    if (lane == 0) {
+      constexpr int kIn = C::kOutInflight;
+      int64_t n = 0;
+      bool ok = true;
+      for (int64_t i = 0; ok; ++i) {
+        if (BWD && t_begin + i >= t_end) break;
+        const int64_t tb = t_begin + i;
+        const int nk = BWD ? decode_tile<BWD>(p, tb).nch : 1;  // forward: one chunk per hand-off
+        for (int kk = 0; kk < nk; ++kk, ++n) {
+          const int b = static_cast<int>(n % OB);
+          if (!wait_bar(bar_ob_full(b), static_cast<uint32_t>((n / OB) & 1), abort_flag,
+                        (kRoleStore << 8) | kBarOut)) {
+            ok = false;
+            break;
+          }
+          const int64_t t = BWD ? tb : static_cast<int64_t>(ob_tile[b]);
+          if (!BWD && t < 0) {
+            ok = false;
+            break;
+          }
+          const int k = BWD ? kk : ob_chunk[b];
+          const Tile x = decode_tile<BWD>(p, t);
+          ptx::tma_store_2d(&p.tm_out, out_addr(b), x.c0 + k * kChunkCols, x.row0);
+          ptx::bulk_commit();
+          // keep kIn stores reading; recycle the buffer of the oldest finished one
+          if (n >= kIn - 1) {
+            ptx::bulk_wait_read<kIn - 1>();
+            ptx::mbar_arrive(bar_ob_empty(static_cast<int>((n - (kIn - 1)) % OB)));
+          }
+        }
+      }
+      ptx::bulk_wait<0>();
     }
   } else {
     // ---------------------------------------------------------- X = invrope(O) on the pe chunk (bwd)
@@ -622,22 +765,35 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::kTmemCols);
   }
+  if (!BWD && threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+      p.sched[0] = 0u;
+      p.sched[1] = 0u;
+      __threadfence();
+    }
+  }
 }
 
-// dM[idx] = sum_c ws[c][idx] over the CTAs' partials in CTA order, with a
-// compensated (Kahan) fp32 sum: deterministic and close to an fp64 sum.
-__global__ void dm_reduce_kernel(const float* __restrict__ ws, float* __restrict__ dM, int nparts,
-                                 int nn) {
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= nn) return;
-  float s = 0.f, comp = 0.f;
-  for (int c = 0; c < nparts; ++c) {
-    const float y = ws[static_cast<int64_t>(c) * nn + idx] - comp;
-    const float t = s + y;
-    comp = (t - s) - y;
-    s = t;
+// dM[idx] = sum over the CTA partials ws[c][idx] in a fixed order: thread row ty
+// sums c = ty, ty+8, ... in fp64, then row 0 adds the 8 row sums in order.
+constexpr int kReduceRows = 8;
+
+__global__ void __launch_bounds__(32 * kReduceRows)
+    dm_reduce_kernel(const float* __restrict__ ws, float* __restrict__ dM, int nparts, int nn) {
+  __shared__ double part[kReduceRows][32];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int idx = blockIdx.x * 32 + tx;
+  double s = 0.0;
+  if (idx < nn)
+    for (int c = ty; c < nparts; c += kReduceRows) s += static_cast<double>(ws[static_cast<int64_t>(c) * nn + idx]);
+  part[ty][tx] = s;
+  __syncthreads();
+  if (ty == 0 && idx < nn) {
+    double t = 0.0;
+    for (int k = 0; k < kReduceRows; ++k) t += part[k][tx];
+    dM[idx] = static_cast<float>(t);
   }
-  dM[idx] = s;
 }
 
 // ---------------------------------------------------------------- host side
@@ -704,6 +860,24 @@ int ensure_smem_attr(int device) {
 
 bool valid_theta(double theta) { return std::isfinite(theta) && theta > 0.0; }
 
+// This launch's schedule counters on the current device: the address of
+// g_sched is looked up once per device; slots rotate per launch.
+int sched_slot(int device, unsigned int** out) {
+  static std::mutex mu;
+  static unsigned int* base[64] = {};
+  static unsigned int seq[64] = {};
+  if (device < 0 || device >= 64) return INVROPE_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!base[device]) {
+    void* ptr = nullptr;
+    const cudaError_t err = cudaGetSymbolAddress(&ptr, g_sched);
+    if (err != cudaSuccess) return cuda_fail(err);
+    base[device] = static_cast<unsigned int*>(ptr);
+  }
+  *out = base[device] + 2 * (seq[device]++ % kSchedSlots);
+  return INVROPE_OK;
+}
+
 }  // namespace
 
 // Grid size of the backward kernel (one dM partial per CTA).
@@ -735,6 +909,7 @@ extern "C" int invrope_postmix_fwd(const void* O, const float* M, void* Y, int64
   p.tm_in1 = p.tm_in0;
   p.M = M;
   p.ws = nullptr;
+  if ((st = sched_slot(dev.device, &p.sched)) != INVROPE_OK) return st;
   p.sq = sq;
   p.pos0 = pos0;
   p.n_tiles = s.n_tiles;
@@ -810,8 +985,8 @@ extern "C" int invrope_postmix_bwd(const void* dY, const void* O, const float* M
     postmix_kernel<true><<<static_cast<unsigned>(grid), KCfg<true>::kThreads, KCfg<true>::kSmemAlloc, cs>>>(p);
     if ((st = check_launch()) != INVROPE_OK) return st;
   }
-  dm_reduce_kernel<<<(nn + 127) / 128, 128, 0, cs>>>(static_cast<const float*>(workspace), dM,
-                                                     static_cast<int>(grid), nn);
+  dm_reduce_kernel<<<(nn + 31) / 32, 32 * kReduceRows, 0, cs>>>(static_cast<const float*>(workspace), dM,
+                                                                 static_cast<int>(grid), nn);
   return check_launch();
 }
 
