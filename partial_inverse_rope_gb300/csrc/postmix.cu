@@ -109,6 +109,7 @@ struct PostmixParams {
   const float* M;
   float* ws;           // bwd: per-CTA dM partials [gridDim.x][nh][nh]
   unsigned int* sched; // fwd: this launch's {next tile, finished CTAs} counters
+  uint64_t F[kMaxHalf];  // rotary frequencies in turns per position, 0.64 fixed point
   int64_t sq;
   int64_t pos0;
   int64_t n_tiles;
@@ -128,8 +129,11 @@ template <bool BWD>
 __device__ __forceinline__ Tile decode_tile(const PostmixParams& p, int64_t t) {
   using C = KCfg<BWD>;
   Tile x;
-  x.rt = static_cast<int>(t / p.n_ct);
-  x.ct = static_cast<int>(t - static_cast<int64_t>(x.rt) * p.n_ct);
+  // 32-bit division: the host guarantees n_tiles < 2^31 (64-bit division here
+  // sits on the MMA issuer's critical path once per tile and is slow)
+  const uint32_t tu = static_cast<uint32_t>(t);
+  x.rt = static_cast<int>(tu / static_cast<uint32_t>(p.n_ct));
+  x.ct = static_cast<int>(tu - static_cast<uint32_t>(x.rt) * static_cast<uint32_t>(p.n_ct));
   x.row0 = x.rt * p.R;
   x.c0 = x.ct * C::NC;
   const int left = p.d - x.c0;
@@ -218,16 +222,26 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
-// A_blk(i, j): blockdiag_P(M) (forward) or blockdiag_P(M^T) (backward), zero
-// outside the R x R block diagonal.
+// Row m of A = blockdiag_P(M) (forward) or blockdiag_P(M^T) (backward): its
+// only nonzero columns are j in [b0, b0 + nh), b0 = (m / nh) * nh, for m < R.
 template <bool BWD>
-__device__ __forceinline__ float a_blk(const PostmixParams& p, int i, int j) {
-  if (i < p.R && j < p.R && (i / p.nh) == (j / p.nh)) {
-    const int gi = i % p.nh, gj = j % p.nh;
-    return BWD ? __ldg(p.M + gj * p.nh + gi) : __ldg(p.M + gi * p.nh + gj);
+struct ARow {
+  const float* M;  // M staged in shared memory
+  int nh, b0, gi;
+  bool live;
+  __device__ __forceinline__ ARow(const PostmixParams& p, const float* Ms, int m) : M(Ms), nh(p.nh) {
+    live = m < p.R;
+    const int blk = live ? m / p.nh : 0;
+    b0 = blk * p.nh;
+    gi = m - b0;
   }
-  return 0.f;
-}
+  __device__ __forceinline__ float at(int j) const {
+    const unsigned gj = static_cast<unsigned>(j - b0);
+    if (!live || gj >= static_cast<unsigned>(nh)) return 0.f;
+    // staged with row stride nh + 1: lanes (consecutive gi) hit distinct banks
+    return BWD ? M[gj * (nh + 1) + gi] : M[gi * (nh + 1) + gj];
+  }
+};
 
 template <bool BWD>
 __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
@@ -305,15 +319,28 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
     ptx::tmem_alloc(base + C::kOffMisc, C::kTmemCols);
     ptx::tmem_relinquish();
   }
-  // Zero the input ring (rows >= R are never loaded and must read as 0) and X_lo.
-  for (uint32_t o = threadIdx.x * 16u; o < static_cast<uint32_t>(S * C::kStageBytes); o += blockDim.x * 16u)
-    ptx::st_shared_v4(base + C::kOffStage + o, 0u, 0u, 0u, 0u);
   if (BWD)
     for (uint32_t o = threadIdx.x * 16u; o < static_cast<uint32_t>(kChunkBytes); o += blockDim.x * 16u)
       ptx::st_shared_v4(base + C::kOffXlo + o, 0u, 0u, 0u, 0u);
-  if (threadIdx.x < half) {
-    const double f = pow(p.theta, -2.0 * static_cast<double>(threadIdx.x) / p.pe);
-    F[threadIdx.x] = __double2ull_rn(f * 0.15915494309189535 * 18446744073709551616.0);
+  if (threadIdx.x < half) F[threadIdx.x] = p.F[threadIdx.x];
+  // M staged in the (still idle) input ring for the A build below, row stride
+  // nh + 1; four independent loads in flight per thread
+  float* Ms = reinterpret_cast<float*>(gbase + C::kOffStage);
+  {
+    const int nn = p.nh * p.nh;
+    for (int k0 = threadIdx.x; k0 < nn; k0 += 4 * blockDim.x) {
+      float v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k = k0 + u * blockDim.x;
+        v[u] = k < nn ? __ldg(p.M + k) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k = k0 + u * blockDim.x;
+        if (k < nn) Ms[(k / p.nh) * (p.nh + 1) + k % p.nh] = v[u];
+      }
+    }
   }
   ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
@@ -327,13 +354,14 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
     const uint32_t quad = static_cast<uint32_t>(warp & 3);
     const int m = static_cast<int>(quad * 32) + lane;
     const uint32_t row_addr = tmem_base + ((quad * 32u) << 16) + C::kACol;
+    const ARow<BWD> arow(p, Ms, m);
     for (int hl = 0; hl < 2; ++hl)
       for (int kh = 0; kh < 2; ++kh) {
         uint32_t w[32];
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
           const int j = kh * 64 + 2 * q;
-          const float v0 = a_blk<BWD>(p, m, j), v1 = a_blk<BWD>(p, m, j + 1);
+          const float v0 = arow.at(j), v1 = arow.at(j + 1);
           const uint32_t h = ptx::pack_bf16x2(v0, v1);
           w[q] = hl == 0 ? h : ptx::pack_bf16x2(v0 - ptx::bf16_lo_f32(h), v1 - ptx::bf16_hi_f32(h));
         }
@@ -341,6 +369,16 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
       }
     ptx::tmem_st_wait();
   }
+  __syncthreads();  // the staged M is dead from here on
+  // Rows >= R of every 64-channel box are never loaded and must read as 0
+  // (the MMA's K range covers them); X_lo starts at 0 on its nope channels.
+  if (p.R < kRowsMax) {
+    const uint32_t tail = static_cast<uint32_t>(kRowsMax - p.R) * 128u;  // bytes per box
+    const uint32_t nbox = static_cast<uint32_t>(S * C::kStageBytes / kChunkBytes);
+    for (uint32_t o = threadIdx.x * 16u; o < nbox * tail; o += blockDim.x * 16u)
+      ptx::st_shared_v4(base + C::kOffStage + (o / tail) * kChunkBytes + p.R * 128u + (o % tail), 0u, 0u, 0u, 0u);
+  }
+  ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -354,9 +392,9 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
     if (lane == 0) {
       // forward: tiles are claimed from the launch's counter, one claim ahead
       int64_t t_next = BWD ? t_begin : static_cast<int64_t>(atomicAdd(p.sched, 1u));
-      for (int64_t i = 0;; ++i) {
+      for (uint32_t i = 0;; ++i) {
         const int st = static_cast<int>(i % S);
-        const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
+        const uint32_t ph = (i / S) & 1u;
         if (BWD && t_next >= t_end) break;
         if (!wait_bar(bar_empty(st), ph ^ 1u, abort_flag, (kRoleProducer << 8) | kBarEmpty)) break;
         const int64_t t = t_next;
@@ -389,11 +427,11 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
       const uint32_t nks = static_cast<uint32_t>((p.R + 15) / 16);
       uint32_t d2_started = 0;
       int npe = 0;
-      for (int64_t i = 0;; ++i) {
+      for (uint32_t i = 0;; ++i) {
         const int st = static_cast<int>(i % S);
-        const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
+        const uint32_t ph = (i / S) & 1u;
         const int acc = static_cast<int>(i % NA);
-        const uint32_t aph = static_cast<uint32_t>((i / NA) & 1);
+        const uint32_t aph = (i / NA) & 1u;
         if (BWD && t_begin + i >= t_end) break;
         if (!wait_bar(bar_full(st), ph, abort_flag, (kRoleMma << 8) | kBarFull)) break;
         const int64_t t = BWD ? t_begin + i : static_cast<int64_t>(stage_tile[st]);
@@ -470,12 +508,12 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
     const int pl = row_ok ? r / p.nh : 0;
     float2* tab = reinterpret_cast<float2*>(gbase + C::kOffTabEpi);
     const float sgn = BWD ? 1.f : -1.f;  // rope (+a) for dO, inverse rope (-a) for Y
-    int64_t n = 0;  // output chunk counter (output ring position)
+    uint32_t n = 0;  // output chunk counter (output ring position)
     bool ok = true;
-    for (int64_t i = 0; ok; ++i) {
+    for (uint32_t i = 0; ok; ++i) {
       if (BWD && t_begin + i >= t_end) break;
       const int acc = static_cast<int>(i % NA);
-      const uint32_t aph = static_cast<uint32_t>((i / NA) & 1);
+      const uint32_t aph = (i / NA) & 1u;
       if (!group_wait(bar_acc_full(acc), aph, abort_flag, (kRoleEpilogue << 8) | kBarAccFull, e == 0,
                       slot_epi + (i & 1), 1))
         break;
@@ -484,7 +522,7 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
       if (!BWD && t < 0) {
         // pass the end of the tile stream on to the store warp
         const int b = static_cast<int>(n % OB);
-        if (group_wait(bar_ob_empty(b), static_cast<uint32_t>(((n / OB) & 1) ^ 1), abort_flag,
+        if (group_wait(bar_ob_empty(b), ((n / OB) & 1u) ^ 1u, abort_flag,
                        (kRoleEpilogue << 8) | kBarOut, e == 0, slot_ob + (n & 1), 1)) {
           if (e == 0) ob_tile[b] = -1;
           ptx::mbar_arrive(bar_ob_full(b));
@@ -500,7 +538,7 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
       const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * C::NC);
       for (int k = 0; k < x.nch; ++k, ++n) {
         const int b = static_cast<int>(n % OB);
-        if (!group_wait(bar_ob_empty(b), static_cast<uint32_t>(((n / OB) & 1) ^ 1), abort_flag,
+        if (!group_wait(bar_ob_empty(b), ((n / OB) & 1u) ^ 1u, abort_flag,
                         (kRoleEpilogue << 8) | kBarOut, e == 0, slot_ob + (n & 1), 1)) {
           ok = false;
           break;
@@ -643,15 +681,15 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
     // ---------------------------------------------------------- TMA store (output ring)
     if (lane == 0) {
       constexpr int kIn = C::kOutInflight;
-      int64_t n = 0;
+      uint32_t n = 0;
       bool ok = true;
-      for (int64_t i = 0; ok; ++i) {
+      for (uint32_t i = 0; ok; ++i) {
         if (BWD && t_begin + i >= t_end) break;
         const int64_t tb = t_begin + i;
         const int nk = BWD ? decode_tile<BWD>(p, tb).nch : 1;  // forward: one chunk per hand-off
         for (int kk = 0; kk < nk; ++kk, ++n) {
           const int b = static_cast<int>(n % OB);
-          if (!wait_bar(bar_ob_full(b), static_cast<uint32_t>((n / OB) & 1), abort_flag,
+          if (!wait_bar(bar_ob_full(b), (n / OB) & 1u, abort_flag,
                         (kRoleStore << 8) | kBarOut)) {
             ok = false;
             break;
@@ -680,12 +718,12 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
       const int xr = threadIdx.x - 192;
       float2* tab = reinterpret_cast<float2*>(gbase + C::kOffTabXf);
       int npe = 0;
-      int64_t i = 0;
+      uint32_t i = 0;
       for (int64_t t = t_begin; t < t_end; ++t, ++i) {
         const Tile x = decode_tile<BWD>(p, t);
         if (!x.has_pe) continue;
         const int st = static_cast<int>(i % S);
-        const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
+        const uint32_t ph = (i / S) & 1u;
         // Wait for the MMA thread's hand-off first: waiting on full[st] directly
         // could match a phase of the stage's previous tile (parity aliasing).
         if (!group_wait(bar_x_go, static_cast<uint32_t>(npe & 1), abort_flag, (kRoleTransform << 8) | kBarXGo,
@@ -824,6 +862,15 @@ bool make_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int d, int box_row
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Rotary frequency f_i = theta^(-2i/pe) as turns per position in 0.64 fixed
+// point: the kernel reduces pos * F[i] mod 2^64 exactly to a fractional turn.
+void fill_freq(uint64_t* F, int pe, double theta) {
+  for (int i = 0; i < pe / 2 && i < kMaxHalf; ++i) {
+    const double f = std::pow(theta, -2.0 * i / pe);
+    F[i] = static_cast<uint64_t>(std::llround(std::ldexp(f * 0.15915494309189535, 63))) << 1;
+  }
+}
+
 struct Shape {
   int P, R, n_ct;
   int64_t n_tiles;
@@ -840,6 +887,7 @@ int check_shape(int64_t sq, int nh, int nope, int pe, int nc, Shape* s) {
   s->R = s->P * nh;
   s->n_ct = static_cast<int>((d + nc - 1) / nc);
   s->n_tiles = ((sq + s->P - 1) / s->P) * s->n_ct;
+  if (s->n_tiles >= (int64_t(1) << 31)) return INVROPE_ERR_UNSUPPORTED;
   return INVROPE_OK;
 }
 
@@ -921,6 +969,7 @@ extern "C" int invrope_postmix_fwd(const void* O, const float* M, void* Y, int64
   p.P = s.P;
   p.R = s.R;
   p.n_ct = s.n_ct;
+  fill_freq(p.F, pe, theta);
   const int64_t grid = s.n_tiles < dev.sms ? s.n_tiles : dev.sms;
   postmix_kernel<false><<<static_cast<unsigned>(grid), KCfg<false>::kThreads, KCfg<false>::kSmemAlloc,
                           reinterpret_cast<cudaStream_t>(stream)>>>(p);
@@ -982,6 +1031,7 @@ extern "C" int invrope_postmix_bwd(const void* dY, const void* O, const float* M
     p.P = s.P;
     p.R = s.R;
     p.n_ct = s.n_ct;
+    fill_freq(p.F, pe, theta);
     postmix_kernel<true><<<static_cast<unsigned>(grid), KCfg<true>::kThreads, KCfg<true>::kSmemAlloc, cs>>>(p);
     if ((st = check_launch()) != INVROPE_OK) return st;
   }
