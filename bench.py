@@ -89,14 +89,16 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (host time, csv line)
         self.thread = None
+        self.t_start = None
+        self.t_stop = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -107,7 +109,13 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark_start(self):
+        self.t_start = time.perf_counter()
+
+    def mark_stop(self):
+        self.t_stop = time.perf_counter()
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -123,7 +131,9 @@ class ClockSampler:
     def summary(self):
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        window = [ln for t, ln in self.lines
+                  if self.t_start is None or self.t_start <= t <= (self.t_stop or t)]
+        for line in window:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 8:
                 continue
@@ -185,11 +195,13 @@ def run_ours(args, rank, world, local):
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        clocks.mark_start()
         t0.record(stream)
         for k in range(args.steps):
             step(k, events[k])
         t1.record(stream)
         torch.cuda.synchronize()
+        clocks.mark_stop()
     barrier(world)
     ms_total = t0.elapsed_time(t1)
     fwd_us = [e[0].elapsed_time(e[1]) * 1e3 for e in events]
@@ -200,7 +212,7 @@ def run_ours(args, rank, world, local):
 
     step_bytes = c.fwd_bytes() + c.bwd_bytes() + R.bytes()
     ms_per_step = ms_total / args.steps
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9  # GB/s over all ranks
+    value = whole_job_gbs(step_bytes, ms_per_step, world)  # GB/s over all ranks
 
     # end to end through the public API with host buffers: pinned host -> device
     # inputs, the three calls, device -> pinned host outputs, all inside the timed region
@@ -307,7 +319,7 @@ def run_e2e(args, ir, c, R, dev, stream, O, dY, Ms, idx, Y, dO, dM, ws, out, wor
     step_bytes = c.fwd_bytes() + c.bwd_bytes() + R.bytes()
     h2d = hO.numel() * 2 + hdY.numel() * 2 + c.nh * c.nh * 4 + hidx.numel() * 4
     d2h = hY.numel() * 2 + hdO.numel() * 2 + c.nh * c.nh * 4 + hout.numel() * 4
-    return {"value": round(world * step_bytes / (dt * 1e-3) / 1e9, 1), "unit": "GB/s",
+    return {"value": round(whole_job_gbs(step_bytes, dt, world), 1), "unit": "GB/s",
             "ms_per_step": round(dt, 3), "steps": steps,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
@@ -319,12 +331,20 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """Largest value of ``x`` over all ranks (the slowest replica's time)."""
     if world <= 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_gbs(step_bytes, ms_per_step_max, world):
+    """Weak-scaling aggregate: every replica moves ``step_bytes`` per step; the
+    job's rate is all ranks' bytes over the slowest rank's time per step."""
+    return world * step_bytes / (ms_per_step_max * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------- oracle (CPU) legs
@@ -371,7 +391,7 @@ def oracle_threads():
 
 
 def cpu_baseline(args):
-    rows = int(os.environ.get("INVROPE_ORACLE_ROWS", "1024"))
+    rows = int(os.environ.get("INVROPE_ORACLE_ROWS", "16384"))
     dt, nbytes, rows, idx_rows = oracle_sample(rows)
     return {"value": round(nbytes / dt / 1e9, 3), "unit": "GB/s", "cores": oracle_threads(),
             "kind": "oracle",
@@ -423,7 +443,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=37)
+    ap.add_argument("--steps", type=int, default=370)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     args = ap.parse_args()

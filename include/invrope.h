@@ -200,6 +200,18 @@ int kv_idx_local_to_global(const int32_t* idx, int32_t* out,
  */
 int invrope_take_device_fault(int* fault);
 
+/*
+ * Watchdog self-test: launches one thread block whose only mbarrier wait can
+ * never complete (nothing arrives on it) and whose bounded wait gives up after
+ * limit_us microseconds (1000..2000000), exactly as the kernels' waits do
+ * after about two seconds. Synchronises the current device before and after;
+ * returns in *fault the code the watchdog recorded, which must be
+ * INVROPE_WATCHDOG_SELFTEST_CODE, and leaves the flag cleared and the CUDA
+ * context usable. Library infrastructure, not an operation of the pages.
+ */
+#define INVROPE_WATCHDOG_SELFTEST_CODE 0x60A
+int invrope_watchdog_selftest(int64_t limit_us, int* fault);
+
 #ifdef __cplusplus
 } /* extern "C" */
 #endif

@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     invrope_postmix_bwd_workspace_bytes,
     invrope_postmix_fwd,
     invrope_take_device_fault,
+    invrope_watchdog_selftest,
     kv_idx_local_to_global,
     lib,
     lib_path,

@@ -49,7 +49,10 @@ _SIGNATURES = {
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
         ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),
     "invrope_take_device_fault": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int)]),
+    "invrope_watchdog_selftest": (ctypes.c_int, [ctypes.c_int64, ctypes.POINTER(ctypes.c_int)]),
 }
+
+INVROPE_WATCHDOG_SELFTEST_CODE = 0x60A
 
 
 class InvropeError(RuntimeError):
@@ -202,4 +205,11 @@ def invrope_take_device_fault() -> int:
     """Synchronise, then return and clear the kernels' watchdog code (0 = no fault)."""
     v = ctypes.c_int(0)
     _check(lib().invrope_take_device_fault(ctypes.byref(v)), "invrope_take_device_fault")
+    return v.value
+
+
+def invrope_watchdog_selftest(limit_us: int = 50000) -> int:
+    """Run one bounded wait that must expire; returns the recorded watchdog code."""
+    v = ctypes.c_int(0)
+    _check(lib().invrope_watchdog_selftest(int(limit_us), ctypes.byref(v)), "invrope_watchdog_selftest")
     return v.value

@@ -149,20 +149,40 @@ __device__ __forceinline__ void record_fault(unsigned code, volatile int* abort_
 }
 
 // Bounded wait on an mbarrier phase. Returns false when the CTA is aborting.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                         unsigned code) {
+__device__ __forceinline__ bool wait_bar_for(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             unsigned code, uint64_t limit_ns) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if ((n & 63u) == 0) {
       if (*abort_flag) return false;
-      if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (ptx::globaltimer_ns() - t0 > limit_ns) {
         record_fault(code, abort_flag);
         return false;
       }
     }
   }
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         unsigned code) {
+  return wait_bar_for(bar, parity, abort_flag, code, kWaitLimitNs);
+}
+
+// One thread waits for phase 0 of an mbarrier that nothing ever arrives on:
+// the bounded wait must give up after limit_ns and record the self-test code.
+__global__ void watchdog_selftest_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bar), 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    wait_bar_for(ptx::smem_u32(&bar), 0, &abort_flag, INVROPE_WATCHDOG_SELFTEST_CODE, limit_ns);
 }
 
 // One leader thread of a 128-thread group does the bounded wait; the whole
@@ -1038,6 +1058,18 @@ extern "C" int invrope_postmix_bwd(const void* dY, const void* O, const float* M
   dm_reduce_kernel<<<(nn + 31) / 32, 32 * kReduceRows, 0, cs>>>(static_cast<const float*>(workspace), dM,
                                                                  static_cast<int>(grid), nn);
   return check_launch();
+}
+
+extern "C" int invrope_watchdog_selftest(int64_t limit_us, int* fault) {
+  if (!fault || limit_us < 1000 || limit_us > 2000000) return INVROPE_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  int st = current_device(&dev);
+  if (st != INVROPE_OK) return st;
+  int stale = 0;
+  if ((st = invrope_take_device_fault(&stale)) != INVROPE_OK) return st;  // start from a clear flag
+  watchdog_selftest_kernel<<<1, 32>>>(static_cast<uint64_t>(limit_us) * 1000u);
+  if ((st = check_launch()) != INVROPE_OK) return st;
+  return invrope_take_device_fault(fault);
 }
 
 extern "C" int invrope_take_device_fault(int* fault) {

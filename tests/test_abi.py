@@ -38,7 +38,7 @@ def test_header_declares_the_expected_entry_points():
     assert _declared_functions() == sorted([
         "invrope_last_cuda_error", "invrope_postmix_bwd", "invrope_postmix_bwd_workspace_bytes",
         "invrope_postmix_bwd_noalloc", "invrope_postmix_fwd", "invrope_status_string",
-        "invrope_take_device_fault", "kv_idx_local_to_global"])
+        "invrope_take_device_fault", "invrope_watchdog_selftest", "kv_idx_local_to_global"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -148,3 +148,10 @@ def test_binding_refuses_wrong_dtypes():
         ir.invrope_postmix_fwd(torch.zeros(4, 2, 64), torch.eye(2), 0, 48, 16)
     with pytest.raises(TypeError):
         ir.kv_idx_local_to_global(torch.zeros(4, 4, dtype=torch.int64), 2, 10)
+
+
+def test_watchdog_selftest_rejects_bad_limits(lib):
+    v = ctypes.c_int(7)
+    assert lib.invrope_watchdog_selftest(10, ctypes.byref(v)) == INVALID
+    assert lib.invrope_watchdog_selftest(10**7, ctypes.byref(v)) == INVALID
+    assert lib.invrope_watchdog_selftest(50000, None) == INVALID

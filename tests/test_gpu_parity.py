@@ -8,6 +8,7 @@ import torch
 
 import oracle
 import partial_inverse_rope_gb300 as ir
+from partial_inverse_rope_gb300 import binding
 from gpu_helpers import (assert_bf16_close, assert_dm_close, ensure_built, f64, make_inputs,
                          sample_rows)
 from partial_inverse_rope_gb300 import inputs as W
@@ -259,3 +260,13 @@ def test_remap_config_full_size():
     assert np.array_equal(out.cpu().numpy(), want)
     out2 = ir.kv_idx_local_to_global(idx, c.sq, c.seqlen_kv)
     assert torch.equal(out, out2)
+
+
+# ------------------------------------------------------------------ bounded waits
+def test_watchdog_gives_up_and_context_stays_usable():
+    """A wait that nothing completes must run out, record its code and return;
+    the context keeps working afterwards."""
+    code = ir.invrope_watchdog_selftest(50000)
+    assert code == binding.INVROPE_WATCHDOG_SELFTEST_CODE
+    _full_check(64, 4, 48, 16, seed=11)
+    assert ir.invrope_take_device_fault() == 0
