@@ -27,6 +27,16 @@
 //     to this CTA's share of dM. X = invrope(O) is exact bf16 on the nope
 //     channels; on the pe channels it is split into hi + lo bf16 terms (hi
 //     replaces O in place, lo goes to a side buffer) so dM carries ~16 bits.
+//   * Backward with nh = 64 and the pe block filling one 64-channel chunk
+//     (e.g. 448 + 64): the head mix is instead one chain of four M = 128,
+//     N = 128 MMAs. A = [M^T_hi ; M^T_lo] stacks the two bf16 terms along M
+//     (rows 0-63 hi, 64-127 lo, K = the 64 heads) and B spans both positions
+//     of the tile along N: its second 64-wide N block is the tile's rows
+//     64-127, reached through the descriptor's N-block stride. The epilogue
+//     adds the lo rows to the hi rows; the lo rows pass through the output
+//     buffer as bf16, a rounding of about 2^-9 of a term that is itself about
+//     2^-9 of the result. This is a quarter of the block-diagonal form's MMA
+//     issue, with none of its zero blocks.
 //   * Every wait is bounded (about two seconds); a wait that runs out records
 //     a fault code, raises a CTA-wide abort flag and the CTA winds down.
 #include <cuda.h>
@@ -117,6 +127,7 @@ struct PostmixParams {
   int nh, nope, pe, d;
   int P, R;            // positions and rows per tile
   int n_ct;            // channel tiles
+  int stacked;         // bwd, nh = 64, pe block = one whole chunk: stacked head mix (below)
 };
 
 struct Tile {
@@ -307,6 +318,14 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
   static_assert(S <= 8 && NA <= 8 && OB <= 8, "tile-id slots");
   uint64_t* F = reinterpret_cast<uint64_t*>(gbase + C::kOffFreq);
   const int half = p.pe >> 1;
+  // Accumulator ring: NA accumulators of NC columns, or 2 of 128 columns for the
+  // stacked backward mix (the same 256 TMEM columns).
+  const bool stk = BWD && p.stacked != 0;
+  static_assert(!BWD || NA == 4, "the backward ring is indexed with shifts");
+  const uint32_t na_sh = stk ? 1u : 2u;
+  const uint32_t acc_cols = stk ? 128u : static_cast<uint32_t>(C::NC);
+  auto acc_of = [&](uint32_t i) { return static_cast<int>(BWD ? i & ((1u << na_sh) - 1u) : i % NA); };
+  auto acc_phase = [&](uint32_t i) { return BWD ? (i >> na_sh) & 1u : (i / NA) & 1u; };
 
   // ------------------------------------------------------------ setup
   if (threadIdx.x == 0) {
@@ -374,19 +393,32 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
     const uint32_t quad = static_cast<uint32_t>(warp & 3);
     const int m = static_cast<int>(quad * 32) + lane;
     const uint32_t row_addr = tmem_base + ((quad * 32u) << 16) + C::kACol;
-    const ARow<BWD> arow(p, Ms, m);
-    for (int hl = 0; hl < 2; ++hl)
-      for (int kh = 0; kh < 2; ++kh) {
-        uint32_t w[32];
+    if (BWD && p.stacked) {
+      // stacked A: lane m < 64 holds M^T_hi row m, lane 64 + h holds M^T_lo row h
+      const int h = m & 63;
+      uint32_t w[32];
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          const int j = kh * 64 + 2 * q;
-          const float v0 = arow.at(j), v1 = arow.at(j + 1);
-          const uint32_t h = ptx::pack_bf16x2(v0, v1);
-          w[q] = hl == 0 ? h : ptx::pack_bf16x2(v0 - ptx::bf16_lo_f32(h), v1 - ptx::bf16_hi_f32(h));
-        }
-        ptx::tmem_st_x32(row_addr + hl * 64 + kh * 32, w);
+      for (int q = 0; q < 32; ++q) {
+        const float v0 = Ms[(2 * q) * 65 + h], v1 = Ms[(2 * q + 1) * 65 + h];
+        const uint32_t hw = ptx::pack_bf16x2(v0, v1);
+        w[q] = m < 64 ? hw : ptx::pack_bf16x2(v0 - ptx::bf16_lo_f32(hw), v1 - ptx::bf16_hi_f32(hw));
       }
+      ptx::tmem_st_x32(row_addr, w);
+    } else {
+      const ARow<BWD> arow(p, Ms, m);
+      for (int hl = 0; hl < 2; ++hl)
+        for (int kh = 0; kh < 2; ++kh) {
+          uint32_t w[32];
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            const int j = kh * 64 + 2 * q;
+            const float v0 = arow.at(j), v1 = arow.at(j + 1);
+            const uint32_t h = ptx::pack_bf16x2(v0, v1);
+            w[q] = hl == 0 ? h : ptx::pack_bf16x2(v0 - ptx::bf16_lo_f32(h), v1 - ptx::bf16_hi_f32(h));
+          }
+          ptx::tmem_st_x32(row_addr + hl * 64 + kh * 32, w);
+        }
+    }
     ptx::tmem_st_wait();
   }
   __syncthreads();  // the staged M is dead from here on
@@ -450,8 +482,8 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
       for (uint32_t i = 0;; ++i) {
         const int st = static_cast<int>(i % S);
         const uint32_t ph = (i / S) & 1u;
-        const int acc = static_cast<int>(i % NA);
-        const uint32_t aph = (i / NA) & 1u;
+        const int acc = acc_of(i);
+        const uint32_t aph = acc_phase(i);
         if (BWD && t_begin + i >= t_end) break;
         if (!wait_bar(bar_full(st), ph, abort_flag, (kRoleMma << 8) | kBarFull)) break;
         const int64_t t = BWD ? t_begin + i : static_cast<int64_t>(stage_tile[st]);
@@ -471,13 +503,23 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
         ptx::tc_fence_after();
         const uint32_t sa = stage_addr(st);
         // head mix: D[acc] = A_hi * B + A_lo * B, A in TMEM, B = the tile (MN-major, K = rows)
-        const uint32_t d_acc = tmem_base + static_cast<uint32_t>(acc * C::NC);
-        const uint32_t idesc_mix = ptx::idesc_bf16_f32(128, 64u * x.nch, false, true);
-        for (uint32_t hl = 0; hl < 2; ++hl)
-          for (uint32_t ks = 0; ks < nks; ++ks) {
-            const uint64_t bd = ptx::smem_desc_sw128(sa + ks * 2048, kChunkBytes, 1024);
-            ptx::tc_mma_ts(d_acc, tmem_base + C::kACol + hl * 64 + ks * 8, bd, idesc_mix, (hl | ks) != 0);
+        const uint32_t d_acc = tmem_base + static_cast<uint32_t>(acc) * acc_cols;
+        if (stk) {
+          // stacked: D[128 x 128] = [M^T_hi ; M^T_lo] * [tile rows 0-63 | tile rows 64-127],
+          // K = the 64 heads of a position; N block 1 sits 64 rows (8 KB) below N block 0
+          const uint32_t idesc_stk = ptx::idesc_bf16_f32(128, 128, false, true);
+          for (uint32_t ks = 0; ks < 4; ++ks) {
+            const uint64_t bd = ptx::smem_desc_sw128(sa + ks * 2048, 64 * 128, 1024);
+            ptx::tc_mma_ts(d_acc, tmem_base + C::kACol + ks * 8, bd, idesc_stk, ks != 0);
           }
+        } else {
+          const uint32_t idesc_mix = ptx::idesc_bf16_f32(128, 64u * x.nch, false, true);
+          for (uint32_t hl = 0; hl < 2; ++hl)
+            for (uint32_t ks = 0; ks < nks; ++ks) {
+              const uint64_t bd = ptx::smem_desc_sw128(sa + ks * 2048, kChunkBytes, 1024);
+              ptx::tc_mma_ts(d_acc, tmem_base + C::kACol + hl * 64 + ks * 8, bd, idesc_mix, (hl | ks) != 0);
+            }
+        }
         if (BWD && x.has_pe) {
           if (!wait_bar(bar_x_full, static_cast<uint32_t>(npe & 1), abort_flag, (kRoleMma << 8) | kBarXFull))
             break;
@@ -532,8 +574,8 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
     bool ok = true;
     for (uint32_t i = 0; ok; ++i) {
       if (BWD && t_begin + i >= t_end) break;
-      const int acc = static_cast<int>(i % NA);
-      const uint32_t aph = (i / NA) & 1u;
+      const int acc = acc_of(i);
+      const uint32_t aph = acc_phase(i);
       if (!group_wait(bar_acc_full(acc), aph, abort_flag, (kRoleEpilogue << 8) | kBarAccFull, e == 0,
                       slot_epi + (i & 1), 1))
         break;
@@ -555,7 +597,7 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
         fill_rot_table(tab, F, p.pos0 + x.s0, p.P, half, e, 128);
         ptx::named_bar_sync(1, 128);
       }
-      const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc * C::NC);
+      const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc) * acc_cols;
       for (int k = 0; k < x.nch; ++k, ++n) {
         const int b = static_cast<int>(n % OB);
         if (!group_wait(bar_ob_empty(b), ((n / OB) & 1u) ^ 1u, abort_flag,
@@ -566,92 +608,154 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
         const uint32_t ob = out_addr(b);
         const bool pe_chunk = x.has_pe && (pcol >> 6) == k;
         const bool pe_whole = pe_chunk && half == 32;  // the pe block is exactly this chunk
-        if (!pe_whole) {
-          // one 64-column TMEM load, one wait, then 8 swizzled 16-byte stores
-          uint32_t v[64];
-          ptx::tmem_ld_x64(taddr + k * kChunkCols, v);
-          ptx::tmem_ld_wait(v);
-          if (row_ok) {
+        if (stk) {
+          // Stacked mix: lane h < 64 holds the hi rows of head h, lane 64 + h
+          // its lo rows; D column 64 p + c is channel c of position p, whose
+          // output row is 64 p + h. The lo warps park their terms (bf16) in
+          // the output buffer; the hi warps add them, rotate, round, overwrite.
+          const int h = r & 63;
+          if (quad >= 2) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const uint32_t w0 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]));
-              const uint32_t w1 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]));
-              const uint32_t w2 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]));
-              const uint32_t w3 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7]));
-              ptx::st_shared_v4(swz_unit_addr(ob, r, 8 * u), w0, w1, w2, w3);
-            }
-          }
-        }
-        if (pe_whole) {
-          // pe = 64 filling the chunk: one load brings both halves of every pair
-          const float2* rt = tab + pl * 32;
-          uint32_t v[64];
-          ptx::tmem_ld_x64(taddr + pcol, v);
-          ptx::tmem_ld_wait(v);
-          if (row_ok) {
+            for (int pp = 0; pp < 2; ++pp) {
+              uint32_t v[64];
+              ptx::tmem_ld_x64(taddr + pp * 64, v);
+              ptx::tmem_ld_wait(v);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              uint32_t w1[4], w2[4];
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                float y1[2], y2[2];
-#pragma unroll
-                for (int s2 = 0; s2 < 2; ++s2) {
-                  const int kq = 8 * u + 2 * q + s2;
-                  const float2 cs = rt[kq];
-                  const float x1 = __uint_as_float(v[kq]), x2 = __uint_as_float(v[32 + kq]);
-                  y1[s2] = x1 * cs.x - sgn * x2 * cs.y;
-                  y2[s2] = x2 * cs.x + sgn * x1 * cs.y;
-                }
-                w1[q] = ptx::pack_bf16x2(y1[0], y1[1]);
-                w2[q] = ptx::pack_bf16x2(y2[0], y2[1]);
+              for (int u = 0; u < 8; ++u) {
+                const uint32_t w0 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]));
+                const uint32_t w1 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]));
+                const uint32_t w2 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]));
+                const uint32_t w3 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7]));
+                ptx::st_shared_v4(swz_unit_addr(ob, pp * 64 + h, 8 * u), w0, w1, w2, w3);
               }
-              ptx::st_shared_v4(swz_unit_addr(ob, r, 8 * u), w1[0], w1[1], w1[2], w1[3]);
-              ptx::st_shared_v4(swz_unit_addr(ob, r, 32 + 8 * u), w2[0], w2[1], w2[2], w2[3]);
             }
           }
-        } else if (pe_chunk) {
-          // rotate the pe pairs of the fp32 accumulator, then round once
-          const int qcol = pcol - k * kChunkCols;  // chunk-relative
-          const float2* rt = tab + pl * half;
-          if ((half & 7) == 0) {
-            for (int i0 = 0; i0 < half; i0 += 8) {
-              uint32_t a[8], bb[8];
-              ptx::tmem_ld_x8(taddr + pcol + i0, a);
-              ptx::tmem_ld_x8(taddr + pcol + half + i0, bb);
-              ptx::tmem_ld_wait(a, bb);
-              if (row_ok) {
+          ptx::named_bar_sync(3, 128);  // the lo terms are in the output buffer
+          if (quad < 2) {
+#pragma unroll 1
+            for (int pp = 0; pp < 2; ++pp) {
+              uint32_t v[64];
+              ptx::tmem_ld_x64(taddr + pp * 64, v);
+              ptx::tmem_ld_wait(v);
+              const int row = pp * 64 + h;
+              float y[64];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                uint32_t l[4];
+                ptx::ld_shared_v4(swz_unit_addr(ob, row, 8 * u), l[0], l[1], l[2], l[3]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  y[8 * u + 2 * q] = __uint_as_float(v[8 * u + 2 * q]) + ptx::bf16_lo_f32(l[q]);
+                  y[8 * u + 2 * q + 1] = __uint_as_float(v[8 * u + 2 * q + 1]) + ptx::bf16_hi_f32(l[q]);
+                }
+              }
+              if (pe_chunk) {
+                // the chunk is the whole pe block: pairs (i, 32 + i)
+                const float2* rt = tab + pp * 32;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                  const float2 cs = rt[i];
+                  const float x1 = y[i], x2 = y[32 + i];
+                  y[i] = x1 * cs.x - sgn * x2 * cs.y;
+                  y[32 + i] = x2 * cs.x + sgn * x1 * cs.y;
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                ptx::st_shared_v4(swz_unit_addr(ob, row, 8 * u), ptx::pack_bf16x2(y[8 * u + 0], y[8 * u + 1]),
+                                  ptx::pack_bf16x2(y[8 * u + 2], y[8 * u + 3]),
+                                  ptx::pack_bf16x2(y[8 * u + 4], y[8 * u + 5]),
+                                  ptx::pack_bf16x2(y[8 * u + 6], y[8 * u + 7]));
+            }
+          }
+        } else {
+          if (!pe_whole) {
+            // one 64-column TMEM load, one wait, then 8 swizzled 16-byte stores
+            uint32_t v[64];
+            ptx::tmem_ld_x64(taddr + k * kChunkCols, v);
+            ptx::tmem_ld_wait(v);
+            if (row_ok) {
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const uint32_t w0 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]));
+                const uint32_t w1 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]));
+                const uint32_t w2 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]));
+                const uint32_t w3 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7]));
+                ptx::st_shared_v4(swz_unit_addr(ob, r, 8 * u), w0, w1, w2, w3);
+              }
+            }
+          }
+          if (pe_whole) {
+            // pe = 64 filling the chunk: one load brings both halves of every pair
+            const float2* rt = tab + pl * 32;
+            uint32_t v[64];
+            ptx::tmem_ld_x64(taddr + pcol, v);
+            ptx::tmem_ld_wait(v);
+            if (row_ok) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
                 uint32_t w1[4], w2[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                   float y1[2], y2[2];
 #pragma unroll
                   for (int s2 = 0; s2 < 2; ++s2) {
-                    const int kq = 2 * q + s2;
-                    const float2 cs = rt[i0 + kq];
-                    const float x1 = __uint_as_float(a[kq]), x2 = __uint_as_float(bb[kq]);
+                    const int kq = 8 * u + 2 * q + s2;
+                    const float2 cs = rt[kq];
+                    const float x1 = __uint_as_float(v[kq]), x2 = __uint_as_float(v[32 + kq]);
                     y1[s2] = x1 * cs.x - sgn * x2 * cs.y;
                     y2[s2] = x2 * cs.x + sgn * x1 * cs.y;
                   }
                   w1[q] = ptx::pack_bf16x2(y1[0], y1[1]);
                   w2[q] = ptx::pack_bf16x2(y2[0], y2[1]);
                 }
-                ptx::st_shared_v4(swz_unit_addr(ob, r, qcol + i0), w1[0], w1[1], w1[2], w1[3]);
-                ptx::st_shared_v4(swz_unit_addr(ob, r, qcol + half + i0), w2[0], w2[1], w2[2], w2[3]);
+                ptx::st_shared_v4(swz_unit_addr(ob, r, 8 * u), w1[0], w1[1], w1[2], w1[3]);
+                ptx::st_shared_v4(swz_unit_addr(ob, r, 32 + 8 * u), w2[0], w2[1], w2[2], w2[3]);
               }
             }
-          } else {
-            for (int ii = 0; ii < half; ++ii) {
-              uint32_t a, bb;
-              ptx::tmem_ld_x1(taddr + pcol + ii, a);
-              ptx::tmem_ld_x1(taddr + pcol + half + ii, bb);
-              ptx::tmem_ld_wait(a, bb);
-              if (row_ok) {
-                const float2 cs = rt[ii];
-                const float x1 = __uint_as_float(a), x2 = __uint_as_float(bb);
-                const int c1 = qcol + ii, c2 = qcol + half + ii;
-                st_shared_b16(swz_unit_addr(ob, r, c1) + (c1 & 7) * 2, bf16_bits(x1 * cs.x - sgn * x2 * cs.y));
-                st_shared_b16(swz_unit_addr(ob, r, c2) + (c2 & 7) * 2, bf16_bits(x2 * cs.x + sgn * x1 * cs.y));
+          } else if (pe_chunk) {
+            // rotate the pe pairs of the fp32 accumulator, then round once
+            const int qcol = pcol - k * kChunkCols;  // chunk-relative
+            const float2* rt = tab + pl * half;
+            if ((half & 7) == 0) {
+              for (int i0 = 0; i0 < half; i0 += 8) {
+                uint32_t a[8], bb[8];
+                ptx::tmem_ld_x8(taddr + pcol + i0, a);
+                ptx::tmem_ld_x8(taddr + pcol + half + i0, bb);
+                ptx::tmem_ld_wait(a, bb);
+                if (row_ok) {
+                  uint32_t w1[4], w2[4];
+#pragma unroll
+                  for (int q = 0; q < 4; ++q) {
+                    float y1[2], y2[2];
+#pragma unroll
+                    for (int s2 = 0; s2 < 2; ++s2) {
+                      const int kq = 2 * q + s2;
+                      const float2 cs = rt[i0 + kq];
+                      const float x1 = __uint_as_float(a[kq]), x2 = __uint_as_float(bb[kq]);
+                      y1[s2] = x1 * cs.x - sgn * x2 * cs.y;
+                      y2[s2] = x2 * cs.x + sgn * x1 * cs.y;
+                    }
+                    w1[q] = ptx::pack_bf16x2(y1[0], y1[1]);
+                    w2[q] = ptx::pack_bf16x2(y2[0], y2[1]);
+                  }
+                  ptx::st_shared_v4(swz_unit_addr(ob, r, qcol + i0), w1[0], w1[1], w1[2], w1[3]);
+                  ptx::st_shared_v4(swz_unit_addr(ob, r, qcol + half + i0), w2[0], w2[1], w2[2], w2[3]);
+                }
+              }
+            } else {
+              for (int ii = 0; ii < half; ++ii) {
+                uint32_t a, bb;
+                ptx::tmem_ld_x1(taddr + pcol + ii, a);
+                ptx::tmem_ld_x1(taddr + pcol + half + ii, bb);
+                ptx::tmem_ld_wait(a, bb);
+                if (row_ok) {
+                  const float2 cs = rt[ii];
+                  const float x1 = __uint_as_float(a), x2 = __uint_as_float(bb);
+                  const int c1 = qcol + ii, c2 = qcol + half + ii;
+                  st_shared_b16(swz_unit_addr(ob, r, c1) + (c1 & 7) * 2, bf16_bits(x1 * cs.x - sgn * x2 * cs.y));
+                  st_shared_b16(swz_unit_addr(ob, r, c2) + (c2 & 7) * 2, bf16_bits(x2 * cs.x + sgn * x1 * cs.y));
+                }
               }
             }
           }
@@ -1051,6 +1155,8 @@ extern "C" int invrope_postmix_bwd(const void* dY, const void* O, const float* M
     p.P = s.P;
     p.R = s.R;
     p.n_ct = s.n_ct;
+    // stacked head mix: two positions of 64 heads per tile, pe block = one chunk
+    p.stacked = (nh == 64 && pe == kChunkCols && nope % kChunkCols == 0) ? 1 : 0;
     fill_freq(p.F, pe, theta);
     postmix_kernel<true><<<static_cast<unsigned>(grid), KCfg<true>::kThreads, KCfg<true>::kSmemAlloc, cs>>>(p);
     if ((st = check_launch()) != INVROPE_OK) return st;

@@ -60,6 +60,8 @@ SHAPES = [
     (1000, 2, 112, 16, 7, 1e4),       # d = 128
     (300, 16, 136, 32, 11, 1e4),      # d = 168: ragged 64-channel chunk, pe inside it
     (257, 64, 0, 64, 0, 1e4),         # nope = 0: every channel rotated
+    (1, 64, 448, 64, 0, 1e4),         # nh = 64 stacked backward mix, one position of two
+    (301, 64, 480, 32, 9, 1e4),       # nh = 64 with pe < 64: block-diagonal backward mix
     (130, 64, 448, 64, 2**31 + 12345, 1e4),  # positions beyond 2^31 (exact angle reduction)
     (33, 128, 448, 64, 0, 5e5),       # 128 heads, another rotary base
     (2053, 16, 448, 64, 0, 1e4),      # mid-like, ragged
