@@ -473,12 +473,49 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
                              x.row0, bar_full(st));
       }
     }
+    __syncwarp();  // the whole warp reaches the teardown barrier together
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t nks = static_cast<uint32_t>((p.R + 15) / 16);
       uint32_t d2_started = 0;
       int npe = 0;
+      // D2 += dY_tile * X_tile^T (both K-major, K = channels), plus dY_pe * X_lo^T on a pe tile
+      auto dm_chain = [&](int st, const Tile& x) {
+        const uint32_t sa = stage_addr(st);
+        const uint32_t d2 = tmem_base + C::kD2Col;
+        const uint32_t idesc_dm = ptx::idesc_bf16_f32(128, 128, false, false);
+        const uint32_t xa = sa + C::kTensorTile;
+        for (int k = 0; k < x.nch; ++k)
+          for (uint32_t kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = ptx::smem_desc_sw128(sa + k * kChunkBytes + kk * 32, 16, 1024);
+            const uint64_t bd = ptx::smem_desc_sw128(xa + k * kChunkBytes + kk * 32, 16, 1024);
+            ptx::tc_mma_ss(d2, ad, bd, idesc_dm, d2_started);
+            d2_started = 1;
+          }
+        if (x.has_pe) {
+          const int kpe = (p.nope - x.c0) / kChunkCols;
+          for (uint32_t kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = ptx::smem_desc_sw128(sa + kpe * kChunkBytes + kk * 32, 16, 1024);
+            const uint64_t bd = ptx::smem_desc_sw128(base + C::kOffXlo + kk * 32, 16, 1024);
+            ptx::tc_mma_ss(d2, ad, bd, idesc_dm, 1);
+          }
+        }
+      };
+      // the pe tile whose dM chain is still to be issued (stage, tile)
+      int pend_st = -1;
+      Tile pend_x{};
+      auto flush_pending = [&]() {
+        if (!wait_bar(bar_x_full, static_cast<uint32_t>(npe & 1), abort_flag, (kRoleMma << 8) | kBarXFull))
+          return false;
+        ptx::tc_fence_after();
+        dm_chain(pend_st, pend_x);
+        ptx::tc_commit(bar_empty(pend_st));
+        ptx::tc_commit(bar_x_empty);
+        ++npe;
+        pend_st = -1;
+        return true;
+      };
       for (uint32_t i = 0;; ++i) {
         const int st = static_cast<int>(i % S);
         const uint32_t ph = (i / S) & 1u;
@@ -520,41 +557,28 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
               ptx::tc_mma_ts(d_acc, tmem_base + C::kACol + hl * 64 + ks * 8, bd, idesc_mix, (hl | ks) != 0);
             }
         }
-        if (BWD && x.has_pe) {
-          if (!wait_bar(bar_x_full, static_cast<uint32_t>(npe & 1), abort_flag, (kRoleMma << 8) | kBarXFull))
-            break;
-          ptx::tc_fence_after();
-        }
-        if (BWD) {
-          // dM share: D2 += dY_tile * X_tile^T (both K-major, K = channels)
-          const uint32_t d2 = tmem_base + C::kD2Col;
-          const uint32_t idesc_dm = ptx::idesc_bf16_f32(128, 128, false, false);
-          const uint32_t xa = sa + C::kTensorTile;
-          for (int k = 0; k < x.nch; ++k)
-            for (uint32_t kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = ptx::smem_desc_sw128(sa + k * kChunkBytes + kk * 32, 16, 1024);
-              const uint64_t bd = ptx::smem_desc_sw128(xa + k * kChunkBytes + kk * 32, 16, 1024);
-              ptx::tc_mma_ss(d2, ad, bd, idesc_dm, d2_started);
-              d2_started = 1;
-            }
-          if (x.has_pe) {
-            const int kpe = (p.nope - x.c0) / kChunkCols;
-            for (uint32_t kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = ptx::smem_desc_sw128(sa + kpe * kChunkBytes + kk * 32, 16, 1024);
-              const uint64_t bd = ptx::smem_desc_sw128(base + C::kOffXlo + kk * 32, 16, 1024);
-              ptx::tc_mma_ss(d2, ad, bd, idesc_dm, 1);
-            }
-          }
-        }
         if (!BWD) acc_tile[acc] = static_cast<int>(t);
-        ptx::tc_commit(bar_acc_full(acc));
-        if (!BWD) ptx::mbar_arrive(bar_acc_full(acc));  // publishes acc_tile[acc]
-        ptx::tc_commit(bar_empty(st));  // the input stage is free once these MMAs are done
-        if (BWD && x.has_pe) {
-          ptx::tc_commit(bar_x_empty);
-          ++npe;
+        ptx::tc_commit(bar_acc_full(acc));  // the epilogue may start once the mix is done
+        if (!BWD) {
+          ptx::mbar_arrive(bar_acc_full(acc));  // publishes acc_tile[acc]
+          ptx::tc_commit(bar_empty(st));        // the input stage is free once the mix is done
+          continue;
+        }
+        // dM share. A pe tile's chain needs the transform warps' X, so it is
+        // issued one tile late, after the next tile's MMAs: the tensor pipe and
+        // the input ring keep moving while X is formed. The issue order is fixed
+        // by the tile sequence alone, so D2 (and dM) stay reproducible.
+        if (!x.has_pe) {
+          dm_chain(st, x);
+          ptx::tc_commit(bar_empty(st));
+        }
+        if (pend_st >= 0 && !flush_pending()) break;
+        if (x.has_pe) {
+          pend_st = st;
+          pend_x = x;
         }
       }
+      if (BWD && pend_st >= 0) flush_pending();
       if (BWD) ptx::tc_commit(bar_d2);
       ptx::tc_commit(bar_done);
       wait_bar(bar_done, 0, abort_flag, (kRoleMma << 8) | kBarDone);
@@ -836,6 +860,7 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
       }
       ptx::bulk_wait<0>();
     }
+    __syncwarp();
   } else {
     // ---------------------------------------------------------- X = invrope(O) on the pe chunk (bwd)
     if (BWD) {
@@ -944,6 +969,7 @@ constexpr int kReduceRows = 8;
 __global__ void __launch_bounds__(32 * kReduceRows)
     dm_reduce_kernel(const float* __restrict__ ws, float* __restrict__ dM, int nparts, int nn) {
   __shared__ double part[kReduceRows][32];
+  ptx::griddep_wait();  // launched early (programmatic dependent launch): wait for the partials
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int idx = blockIdx.x * 32 + tx;
   double s = 0.0;
@@ -1161,8 +1187,23 @@ extern "C" int invrope_postmix_bwd(const void* dY, const void* O, const float* M
     postmix_kernel<true><<<static_cast<unsigned>(grid), KCfg<true>::kThreads, KCfg<true>::kSmemAlloc, cs>>>(p);
     if ((st = check_launch()) != INVROPE_OK) return st;
   }
-  dm_reduce_kernel<<<(nn + 31) / 32, 32 * kReduceRows, 0, cs>>>(static_cast<const float*>(workspace), dM,
-                                                                 static_cast<int>(grid), nn);
+  // Programmatic dependent launch: the reduction grid's launch is processed
+  // while the main kernel drains, and its blocks wait in-kernel (griddepcontrol)
+  // for the main kernel's partials. The main kernel does not signal early:
+  // reduction blocks that start early crowd onto the first SMs to free up.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((nn + 31) / 32));
+  cfg.blockDim = dim3(32 * kReduceRows);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = cs;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = grid > 0 ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, dm_reduce_kernel, static_cast<const float*>(workspace), dM,
+                                             static_cast<int>(grid), nn);
+  if (err != cudaSuccess) return cuda_fail(err);
   return check_launch();
 }
 
