@@ -14,6 +14,10 @@ from .invrope_oracle import (  # noqa: F401
     postmix_fwd,
     postmix_bwd,
     postmix_bwd_dM,
+    postmix_fwd_grouped,
+    postmix_bwd_grouped,
     kv_idx_local_to_global,
+    kv_idx_local_to_global_i64,
     positions_contiguous,
+    positions_batched,
 )

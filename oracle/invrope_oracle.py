@@ -42,7 +42,9 @@ Readings where the pages are silent (each pinned by a closed-form test in
 Array conventions: ``O, dY, Y, dO`` are ``[sq, nh, d]`` with ``d = nope+pe``
 (channel fastest); ``M, dM`` are ``[nh, nh]`` with ``Y[s, g] = sum_h M[g, h]
 X[s, h]``; ``positions`` is an integer array of length ``sq`` holding the
-absolute position of each row (contiguous ``pos0 + s`` for the configs).
+absolute position of each row (contiguous ``pos0 + s`` for the configs, or
+any integers: several folded sequences, a context-parallel rebalance). The
+grouped postmix takes ``Mg`` as ``[nh/gs, gs, gs]``.
 """
 
 from __future__ import annotations
@@ -166,6 +168,58 @@ def postmix_bwd(dY, O, M, positions, nope: int, pe: int, theta: float):
     return dO, dM
 
 
+def _group_slices(nh: int, gs: int):
+    """Head slices of the groups: group ``k`` holds heads ``k*gs .. k*gs+gs-1``."""
+    if gs < 1 or nh % gs:
+        raise ValueError("the group size must divide nh")
+    return [slice(k * gs, (k + 1) * gs) for k in range(nh // gs)]
+
+
+def postmix_fwd_grouped(O, Mg, positions, nope: int, pe: int, theta: float) -> np.ndarray:
+    """Grouped VHA postmix after the inverse RoPE, in fp64.
+
+    [PR1772] Chinese description section 1 and [PR1843] list
+    ``vha_postmix_grouped=True`` among the configurations the fused path
+    leaves to the unfused code; the pages do not spell the grouped mix out.
+    Reading: the heads form ``ng = nh / gs`` groups of ``gs`` consecutive
+    heads, and each group is mixed by its own ``[gs, gs]`` matrix:
+    ``Y[s, k*gs + i, :] = sum_j Mg[k, i, j] * X[s, k*gs + j, :]``, i.e. the
+    ungrouped postmix with a block-diagonal head mix. ``Mg`` is
+    ``[ng, gs, gs]``.
+    """
+    X = invrope(O, positions, nope, pe, theta)
+    Mg = _f64(Mg)
+    ng, gs, gs2 = Mg.shape
+    if gs != gs2 or X.shape[1] != ng * gs:
+        raise ValueError("Mg must be [nh/gs, gs, gs]")
+    Y = np.empty_like(X)
+    for k, sl in enumerate(_group_slices(X.shape[1], gs)):
+        Y[:, sl, :] = np.matmul(Mg[k][None, :, :], X[:, sl, :])
+    return Y
+
+
+def postmix_bwd_grouped(dY, O, Mg, positions, nope: int, pe: int, theta: float):
+    """Backward of :func:`postmix_fwd_grouped`: returns ``(dO, dMg)`` in fp64.
+
+    Per group ``k``: the input gradient ``dX = Mg[k]^T dY`` on the group's
+    heads, rotated back by ``+a`` on the pe channels (as in
+    :func:`postmix_bwd`), and ``dMg[k, i, j] = sum_{s, c} dY[s, k*gs+i, c] *
+    X[s, k*gs+j, c]`` (the weight gradient of [PR1772] Chinese section 1
+    restricted to the pairs of heads that the group's matrix mixes).
+    """
+    Mg = _f64(Mg)
+    ng, gs, _ = Mg.shape
+    dY = np.asarray(dY)
+    O = np.asarray(O)
+    G = np.empty(dY.shape, dtype=np.float64)
+    dMg = np.empty((ng, gs, gs), dtype=np.float64)
+    for k, sl in enumerate(_group_slices(dY.shape[1], gs)):
+        G[:, sl, :] = np.matmul(Mg[k].T[None, :, :], _f64(dY[:, sl, :]))
+        dMg[k] = postmix_bwd_dM(dY[:, sl, :], O[:, sl, :], positions, nope, pe, theta)
+    dO = rope(G, positions, nope, pe, theta)
+    return dO, dMg
+
+
 def kv_idx_local_to_global(idx, sq: int, seqlen_kv: int) -> np.ndarray:
     """Per-batch-local -> flat-global KV column indices, int32 ``[rows, topk]``.
 
@@ -188,6 +242,38 @@ def kv_idx_local_to_global(idx, sq: int, seqlen_kv: int) -> np.ndarray:
     return ((out + 2**31) % 2**32 - 2**31).astype(np.int32)
 
 
+def kv_idx_local_to_global_i64(idx, sq: int, seqlen_kv: int) -> np.ndarray:
+    """The remap of :func:`kv_idx_local_to_global` on an int64 table.
+
+    [PR1772] (the note on the remap tests' host memory) builds the remap
+    tables once per index dtype, with topk widths 640 and 2176. Same rule:
+    ``out = idx + (r // sq) * seqlen_kv`` where ``idx >= 0``, padding
+    (``idx < 0``) unchanged; the addition wraps in 64-bit two's complement.
+    """
+    idx = np.asarray(idx)
+    if idx.ndim != 2:
+        raise ValueError("idx must be [rows, topk]")
+    rows = idx.shape[0]
+    if sq <= 0 or rows % sq:
+        raise ValueError("rows must be a multiple of sq")
+    out = []
+    for r in range(rows):
+        off = (r // sq) * int(seqlen_kv)
+        row = []
+        for v in idx[r].tolist():
+            w = v if v < 0 else v + off
+            row.append((w + 2**63) % 2**64 - 2**63)   # exact Python ints, then wrap
+        out.append(row)
+    return np.array(out, dtype=np.int64).reshape(idx.shape)
+
+
+def positions_batched(b: int, sq_per_batch: int, pos0: int = 0) -> np.ndarray:
+    """Positions of ``b`` sequences of ``sq_per_batch`` tokens folded into one
+    token axis (``B*S`` folding): row ``s`` sits at ``pos0 + s % sq_per_batch``."""
+    s = np.arange(b * sq_per_batch, dtype=np.int64)
+    return pos0 + s % sq_per_batch
+
+
 def positions_contiguous(sq: int, pos0: int) -> np.ndarray:
     """Absolute positions ``pos0 .. pos0+sq-1`` of a contiguous shard."""
     return np.arange(pos0, pos0 + sq, dtype=np.int64)
@@ -195,6 +281,7 @@ def positions_contiguous(sq: int, pos0: int) -> np.ndarray:
 
 __all__ = [
     "inv_freq", "rope_angles", "invrope", "rope", "postmix_fwd",
-    "postmix_bwd", "postmix_bwd_dM", "kv_idx_local_to_global",
-    "positions_contiguous",
+    "postmix_bwd", "postmix_bwd_dM", "postmix_fwd_grouped",
+    "postmix_bwd_grouped", "kv_idx_local_to_global",
+    "kv_idx_local_to_global_i64", "positions_contiguous", "positions_batched",
 ]

@@ -18,7 +18,13 @@ forms, hand-derived integers, invariants and brute force):
   the per-position rotation;
 * backward: the adjoint identity ``<fwd(O), dY> = <O, dO(dY)>``, dM from
   unit matrices (``Y`` is linear in ``M``) and central finite differences;
-* remap: the hand-derived ``golden/kv_remap_small.json`` and brute force.
+* remap: the hand-derived ``golden/kv_remap_small.json`` and brute force;
+  the int64 table the same, plus the 64-bit wrap;
+* grouped postmix: one group equals the ungrouped postmix, several groups
+  equal the ungrouped postmix with the block-diagonal matrix (and dM's
+  diagonal blocks), and pure-Python brute force on a tiny case;
+* folded positions: closed form, and a folded batch equals its sequences
+  run one by one.
 """
 
 from __future__ import annotations
@@ -276,6 +282,113 @@ def check_remap_wraps_int32(impl):
     assert out.tolist() == [[2**30], [-2**31]], out.tolist()
 
 
+# --------------------------------------------------------------------------
+# grouped postmix, arbitrary positions, int64 remap
+# --------------------------------------------------------------------------
+
+def _grouped_case(seed, sq=4, ng=2, gs=3, nope=2, pe=4):
+    r = _rng(seed)
+    nh = ng * gs
+    O = r.standard_normal((sq, nh, nope + pe))
+    dY = r.standard_normal((sq, nh, nope + pe))
+    Mg = np.eye(gs)[None] + 0.3 * r.standard_normal((ng, gs, gs))
+    pos = np.array([3, 0, 9, 4, 1, 6][:sq], dtype=np.int64)
+    return O, dY, Mg, pos, nope, pe, 50.0
+
+
+def _block_diag(Mg):
+    ng, gs, _ = Mg.shape
+    M = np.zeros((ng * gs, ng * gs))
+    for k in range(ng):
+        M[k * gs:(k + 1) * gs, k * gs:(k + 1) * gs] = Mg[k]
+    return M
+
+
+def check_grouped_one_group_is_ungrouped(impl):
+    O, dY, M, pos, nope, pe, theta = _tiny_case(13)
+    _close(impl.postmix_fwd_grouped(O, M[None], pos, nope, pe, theta),
+           impl.postmix_fwd(O, M, pos, nope, pe, theta), what="one group: Y")
+    dO_g, dM_g = impl.postmix_bwd_grouped(dY, O, M[None], pos, nope, pe, theta)
+    dO, dM = impl.postmix_bwd(dY, O, M, pos, nope, pe, theta)
+    _close(dO_g, dO, what="one group: dO")
+    _close(dM_g[0], dM, what="one group: dM")
+
+
+def check_grouped_is_block_diagonal_mix(impl):
+    O, dY, Mg, pos, nope, pe, theta = _grouped_case(14)
+    M = _block_diag(Mg)
+    _close(impl.postmix_fwd_grouped(O, Mg, pos, nope, pe, theta),
+           impl.postmix_fwd(O, M, pos, nope, pe, theta), what="grouped Y")
+    dO_g, dM_g = impl.postmix_bwd_grouped(dY, O, Mg, pos, nope, pe, theta)
+    dO, dM = impl.postmix_bwd(dY, O, M, pos, nope, pe, theta)
+    _close(dO_g, dO, what="grouped dO")
+    gs = Mg.shape[1]
+    for k in range(Mg.shape[0]):
+        sl = slice(k * gs, (k + 1) * gs)
+        _close(dM_g[k], dM[sl, sl], what=f"grouped dM block {k}")
+
+
+def check_grouped_brute_force(impl):
+    O, dY, Mg, pos, nope, pe, theta = _grouped_case(15, sq=2, ng=2, gs=2, nope=1, pe=2)
+    sq, nh, d = O.shape
+    gs = Mg.shape[1]
+    X = np.zeros_like(O)
+    for s in range(sq):
+        a = pos[s] * 1.0          # pe = 2: one pair, f_0 = 1, angle = position
+        for h in range(nh):
+            X[s, h, 0] = O[s, h, 0]
+            X[s, h, 1] = O[s, h, 1] * math.cos(a) + O[s, h, 2] * math.sin(a)
+            X[s, h, 2] = O[s, h, 2] * math.cos(a) - O[s, h, 1] * math.sin(a)
+    Y = np.zeros_like(O)
+    dM = np.zeros_like(Mg)
+    for s in range(sq):
+        for g in range(nh):
+            k, i = divmod(g, gs)
+            for c in range(d):
+                Y[s, g, c] = sum(Mg[k, i, j] * X[s, k * gs + j, c] for j in range(gs))
+                for j in range(gs):
+                    dM[k, i, j] += dY[s, g, c] * X[s, k * gs + j, c]
+    _close(impl.postmix_fwd_grouped(O, Mg, pos, nope, pe, theta), Y, what="brute force grouped Y")
+    _close(impl.postmix_bwd_grouped(dY, O, Mg, pos, nope, pe, theta)[1], dM,
+           what="brute force grouped dM")
+
+
+def check_positions_batched(impl):
+    assert impl.positions_batched(3, 4, 10).tolist() == [10, 11, 12, 13] * 3
+    assert impl.positions_batched(1, 5).tolist() == [0, 1, 2, 3, 4]
+    # folded sequences rotate like the same rows run one sequence at a time
+    O, _, M, _, nope, pe, theta = _tiny_case(16, sq=6, nh=2, nope=2, pe=4)
+    pos = impl.positions_batched(2, 3, 7)
+    Y = impl.postmix_fwd(O, M, pos, nope, pe, theta)
+    for b in range(2):
+        rows = slice(3 * b, 3 * b + 3)
+        _close(Y[rows], impl.postmix_fwd(O[rows], M, impl.positions_contiguous(3, 7), nope, pe, theta),
+               what=f"batch {b}")
+
+
+def check_remap_i64_brute_force(impl):
+    r = _rng(17)
+    b, sq, topk, skv = 3, 4, 5, 3 * 2**40
+    idx = r.integers(0, skv, size=(b * sq, topk)).astype(np.int64)
+    idx[r.random(idx.shape) < 0.2] = -7
+    out = impl.kv_idx_local_to_global_i64(idx, sq, skv)
+    assert out.dtype == np.int64
+    for row in range(b * sq):
+        for k in range(topk):
+            v = int(idx[row, k])
+            want = v if v < 0 else v + (row // sq) * skv
+            assert int(out[row, k]) == want, (row, k, v, int(out[row, k]))
+
+
+def check_remap_i64_wraps_and_matches_i32(impl):
+    out = impl.kv_idx_local_to_global_i64(np.array([[2**62], [2**62]], dtype=np.int64), 1, 2**62)
+    # batch 1: 2^62 + 2^62 = 2^63 wraps to -2^63 in 64-bit two's complement
+    assert out.tolist() == [[2**62], [-2**63]], out.tolist()
+    g = _load("kv_remap_small.json")
+    idx = np.array(g["idx"], dtype=np.int64)
+    assert impl.kv_idx_local_to_global_i64(idx, g["sq"], g["seqlen_kv"]).tolist() == g["out"]
+
+
 ALL_CHECKS = [
     check_inv_freq_closed_forms,
     check_angle_is_position_at_f0,
@@ -294,4 +407,10 @@ ALL_CHECKS = [
     check_remap_golden,
     check_remap_brute_force,
     check_remap_wraps_int32,
+    check_grouped_one_group_is_ungrouped,
+    check_grouped_is_block_diagonal_mix,
+    check_grouped_brute_force,
+    check_positions_batched,
+    check_remap_i64_brute_force,
+    check_remap_i64_wraps_and_matches_i32,
 ]

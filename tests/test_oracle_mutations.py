@@ -115,7 +115,57 @@ def _mutants():
         out = np.where(idx >= 0, idx + b * seqlen_kv, idx)
         return np.clip(out, -2**31, 2**31 - 1).astype(np.int32)
 
+    def grouped_ns(transpose_fwd=False, strided=False, dM_t=False):
+        def groups(nh, gs):
+            ng = nh // gs
+            if strided:  # heads k, k+ng, k+2ng, ... instead of consecutive heads
+                return [np.arange(k, nh, ng) for k in range(ng)]
+            return [np.arange(k * gs, (k + 1) * gs) for k in range(ng)]
+
+        def fwd(O, Mg, positions, nope, pe, theta):
+            X = base.invrope(O, positions, nope, pe, theta)
+            Mg = np.asarray(Mg, dtype=np.float64)
+            Y = np.empty_like(X)
+            for k, hs in enumerate(groups(X.shape[1], Mg.shape[1])):
+                m = Mg[k].T if transpose_fwd else Mg[k]
+                Y[:, hs, :] = np.matmul(m[None], X[:, hs, :])
+            return Y
+
+        def bwd(dY, O, Mg, positions, nope, pe, theta):
+            Mg = np.asarray(Mg, dtype=np.float64)
+            dY = np.asarray(dY, dtype=np.float64)
+            X = base.invrope(O, positions, nope, pe, theta)
+            G = np.empty_like(dY)
+            dM = np.empty_like(Mg)
+            for k, hs in enumerate(groups(dY.shape[1], Mg.shape[1])):
+                G[:, hs, :] = np.matmul(Mg[k].T[None], dY[:, hs, :])
+                blk = np.einsum("sgc,shc->gh", dY[:, hs, :], X[:, hs, :])
+                dM[k] = blk.T if dM_t else blk
+            return base.rope(G, positions, nope, pe, theta), dM
+
+        return _namespace(postmix_fwd_grouped=fwd, postmix_bwd_grouped=bwd)
+
+    def remap64_by_row(idx, sq, seqlen_kv):
+        idx = np.asarray(idx).astype(np.int64)
+        r = np.arange(idx.shape[0])[:, None]
+        return np.where(idx >= 0, idx + r * seqlen_kv, idx)
+
+    def remap64_saturates(idx, sq, seqlen_kv):
+        idx = np.asarray(idx).astype(object)
+        b = (np.arange(idx.shape[0]) // sq)[:, None]
+        out = np.where(idx >= 0, idx + b * int(seqlen_kv), idx)
+        return np.clip(out, -2**63, 2**63 - 1).astype(np.int64)
+
+    def remap64_via_int32(idx, sq, seqlen_kv):
+        return base.kv_idx_local_to_global(np.asarray(idx).astype(np.int32), sq, seqlen_kv).astype(np.int64)
+
     return {
+        "grouped_blocks_transposed": grouped_ns(transpose_fwd=True),
+        "grouped_heads_strided": grouped_ns(strided=True),
+        "grouped_dM_transposed": grouped_ns(dM_t=True),
+        "remap64_offset_by_row": _namespace(kv_idx_local_to_global_i64=remap64_by_row),
+        "remap64_saturates": _namespace(kv_idx_local_to_global_i64=remap64_saturates),
+        "remap64_truncates_to_int32": _namespace(kv_idx_local_to_global_i64=remap64_via_int32),
         "inverse_rotates_forward": _postmix_ns(bad_inv, bad_rope, ok_angles),
         "interleaved_pairs": _postmix_ns(il_inv, il_rope, il_angles),
         "frequency_index_shift": _postmix_ns(fs_inv, fs_rope, fs_angles),
