@@ -139,6 +139,52 @@ int invrope_postmix_bwd(const void* dY, const void* O, const float* M,
                         struct CUstream_st* stream);
 
 /*
+ * Forward with a grouped head mix and/or per-row positions. With gs = nh and
+ * positions = NULL this is exactly invrope_postmix_fwd.
+ *
+ *   Y[s, k*gs + i, :] = sum_j M[k, i, j] * invrope_{p(s)}(O[s, k*gs + j, :])
+ *   p(s) = pos0 + (positions ? positions[s] : s)
+ *
+ * Grouped mix: [PR1772] Chinese section 1 lists vha_postmix_grouped among the
+ *      configurations its fused path hands back to the unfused code, without
+ *      spelling the grouped mix out. It is read here as ng = nh / gs groups of
+ *      gs consecutive heads, each mixed by its own [gs, gs] matrix (a
+ *      block-diagonal [nh, nh] mix).
+ * Positions: [PR1772] English item 1 runs the shard of a context-parallel
+ *      split (positions are then not 0..sq-1), and the token axis may fold
+ *      several sequences (positions restart per sequence); any int32 values
+ *      are accepted, negative ones included (angles are taken mod 2 pi).
+ * M         : fp32 [nh/gs, gs, gs] (row-major), input.
+ * gs        : heads per group, 1 <= gs <= nh, nh % gs == 0.
+ * positions : int32 [sq] DEVICE array, 4-byte aligned, or NULL; pos0 is
+ *             added to every entry (pos0 >= 0).
+ * Other arguments, errors and rounding as in invrope_postmix_fwd.
+ */
+int invrope_postmix_fwd_ex(const void* O, const float* M, void* Y,
+                           int64_t sq, int nh, int gs, int nope, int pe,
+                           const int32_t* positions, int64_t pos0, double theta,
+                           struct CUstream_st* stream);
+
+/*
+ * Backward of invrope_postmix_fwd_ex (gs = nh, positions = NULL: exactly
+ * invrope_postmix_bwd):
+ *
+ *   dO[s, k*gs + j, :] = rope_{p(s)}( sum_i M[k, i, j] * dY[s, k*gs + i, :] )
+ *   dM[k, i, j]        = sum_{s, c} dY[s, k*gs + i, c] * X[s, k*gs + j, c]
+ *
+ * M, dM : fp32 [nh/gs, gs, gs]; dM is overwritten. The workspace is the
+ *         same as for the ungrouped call (invrope_postmix_bwd_workspace_bytes).
+ * Other arguments, errors and determinism as in invrope_postmix_bwd and
+ * invrope_postmix_fwd_ex; positions must not overlap an output.
+ */
+int invrope_postmix_bwd_ex(const void* dY, const void* O, const float* M,
+                           void* dO, float* dM,
+                           void* workspace, size_t workspace_bytes,
+                           int64_t sq, int nh, int gs, int nope, int pe,
+                           const int32_t* positions, int64_t pos0, double theta,
+                           struct CUstream_st* stream);
+
+/*
  * Size of the fixed device scratch that invrope_postmix_bwd_noalloc uses in
  * place of a workspace: 8 MiB, i.e. up to 512 dM partials at nh = 64.
  */
@@ -191,6 +237,21 @@ int invrope_postmix_bwd_noalloc(const void* dY, const void* O, const float* M,
 int kv_idx_local_to_global(const int32_t* idx, int32_t* out,
                            int64_t rows, int topk, int64_t sq,
                            int64_t seqlen_kv, struct CUstream_st* stream);
+
+/*
+ * The same remap on an int64 table ([PR1772]'s remap tests build their tables
+ * once per index dtype):
+ *
+ *   out[r, k] = idx[r, k] < 0 ? idx[r, k] : idx[r, k] + (r / sq) * seqlen_kv
+ *
+ * idx, out : int64 [rows, topk], 8-byte aligned; out may be idx itself.
+ * rows = b * sq, topk >= 0, sq >= 1, seqlen_kv >= 0, and b * seqlen_kv <= 2^63
+ * so that every in-range index maps into int64. Entries >= seqlen_kv are not
+ * clamped; the add wraps in 64-bit two's complement. Bit-exact.
+ */
+int kv_idx_local_to_global_i64(const int64_t* idx, int64_t* out,
+                               int64_t rows, int topk, int64_t sq,
+                               int64_t seqlen_kv, struct CUstream_st* stream);
 
 /*
  * Synchronises the current device, then returns in *fault the watchdog code

@@ -6,12 +6,15 @@ C ABI (``include/invrope.h``), with a thin ctypes binding of the same names.
 from .binding import (  # noqa: F401
     InvropeError,
     invrope_postmix_bwd,
+    invrope_postmix_bwd_ex,
     invrope_postmix_bwd_noalloc,
     invrope_postmix_bwd_workspace_bytes,
     invrope_postmix_fwd,
+    invrope_postmix_fwd_ex,
     invrope_take_device_fault,
     invrope_watchdog_selftest,
     kv_idx_local_to_global,
+    kv_idx_local_to_global_i64,
     lib,
     lib_path,
 )

@@ -45,7 +45,20 @@ _SIGNATURES = {
         ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_int64, ctypes.c_double, ctypes.c_void_p]),
+    "invrope_postmix_fwd_ex": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_double, ctypes.c_void_p]),
+    "invrope_postmix_bwd_ex": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_size_t,
+        ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_double, ctypes.c_void_p]),
     "kv_idx_local_to_global": (ctypes.c_int, [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),
+    "kv_idx_local_to_global_i64": (ctypes.c_int, [
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
         ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),
     "invrope_take_device_fault": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int)]),
@@ -162,6 +175,74 @@ def invrope_postmix_bwd(dY, O, M, pos0: int, nope: int, pe: int, theta: float = 
     return dO, dM
 
 
+def _mix_and_positions(M, positions, sq, nh, group_size, device):
+    """Check the [nh/gs, gs, gs] mix and the optional int32 [sq] positions."""
+    gs = nh if group_size is None else int(group_size)
+    if gs < 1 or nh % gs:
+        raise ValueError("group_size must divide nh")
+    want = (nh // gs, gs, gs) if group_size is not None else (nh, nh)
+    _need(M, "M", torch.float32, len(want))
+    if tuple(M.shape) != want:
+        raise ValueError(f"M must be {list(want)}")
+    if positions is not None:
+        _need(positions, "positions", torch.int32, 1)
+        if positions.shape[0] != sq or positions.device != device:
+            raise ValueError("positions must be int32 [sq] on the tensors' device")
+    return gs, (positions.data_ptr() if positions is not None else None)
+
+
+def invrope_postmix_fwd_ex(O, M, nope: int, pe: int, positions=None, pos0: int = 0,
+                           theta: float = 10000.0, group_size=None, Y=None, stream=None):
+    """Forward with an optional grouped mix (``M`` = [nh/gs, gs, gs] when
+    ``group_size`` is given) and optional int32 per-row ``positions`` (row s
+    sits at ``pos0 + positions[s]``, else ``pos0 + s``); returns ``Y``."""
+    _need(O, "O", torch.bfloat16, 3)
+    sq, nh, d = O.shape
+    gs, pos_ptr = _mix_and_positions(M, positions, sq, nh, group_size, O.device)
+    if Y is None:
+        Y = torch.empty_like(O)
+    else:
+        _need(Y, "Y", torch.bfloat16, 3)
+        if Y.shape != O.shape:
+            raise ValueError("Y must have O's shape")
+    st = lib().invrope_postmix_fwd_ex(O.data_ptr(), M.data_ptr(), Y.data_ptr(), sq, nh, gs, nope, pe,
+                                      pos_ptr, int(pos0), float(theta), _stream_handle(O.device, stream))
+    _check(st, "invrope_postmix_fwd_ex")
+    return Y
+
+
+def invrope_postmix_bwd_ex(dY, O, M, nope: int, pe: int, positions=None, pos0: int = 0,
+                           theta: float = 10000.0, group_size=None, dO=None, dM=None,
+                           workspace=None, stream=None):
+    """Backward of :func:`invrope_postmix_fwd_ex`; returns ``(dO bf16, dM fp32)``
+    with ``dM`` shaped like ``M``."""
+    _need(dY, "dY", torch.bfloat16, 3)
+    _need(O, "O", torch.bfloat16, 3)
+    sq, nh, d = O.shape
+    if dY.shape != O.shape:
+        raise ValueError("dY must match O")
+    gs, pos_ptr = _mix_and_positions(M, positions, sq, nh, group_size, O.device)
+    if dO is None:
+        dO = torch.empty_like(O)
+    if dM is None:
+        dM = torch.empty(M.shape, dtype=torch.float32, device=O.device)
+    _need(dO, "dO", torch.bfloat16, 3)
+    _need(dM, "dM", torch.float32, M.dim())
+    if dM.shape != M.shape:
+        raise ValueError("dM must have M's shape")
+    if workspace is None:
+        nbytes = invrope_postmix_bwd_workspace_bytes(sq, nh, nope, pe)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=O.device)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().invrope_postmix_bwd_ex(dY.data_ptr(), O.data_ptr(), M.data_ptr(), dO.data_ptr(),
+                                      dM.data_ptr(), workspace.data_ptr(), ws_bytes, sq, nh, gs, nope, pe,
+                                      pos_ptr, int(pos0), float(theta), _stream_handle(O.device, stream))
+    _check(st, "invrope_postmix_bwd_ex")
+    return dO, dM
+
+
 def invrope_postmix_bwd_noalloc(dY, O, M, pos0: int, nope: int, pe: int, dO, dM,
                                 theta: float = 10000.0, stream=None):
     """Backward without a workspace, for callers that may not allocate device
@@ -198,6 +279,22 @@ def kv_idx_local_to_global(idx, sq: int, seqlen_kv: int, out=None, stream=None):
     st = lib().kv_idx_local_to_global(idx.data_ptr(), out.data_ptr(), rows, topk, int(sq),
                                       int(seqlen_kv), _stream_handle(idx.device, stream))
     _check(st, "kv_idx_local_to_global")
+    return out
+
+
+def kv_idx_local_to_global_i64(idx, sq: int, seqlen_kv: int, out=None, stream=None):
+    """The same remap on an int64 ``[rows, topk]`` table (64-bit wrap)."""
+    _need(idx, "idx", torch.int64, 2)
+    rows, topk = idx.shape
+    if out is None:
+        out = torch.empty_like(idx)
+    else:
+        _need(out, "out", torch.int64, 2)
+        if out.shape != idx.shape:
+            raise ValueError("out must match idx")
+    st = lib().kv_idx_local_to_global_i64(idx.data_ptr(), out.data_ptr(), rows, topk, int(sq),
+                                          int(seqlen_kv), _stream_handle(idx.device, stream))
+    _check(st, "kv_idx_local_to_global_i64")
     return out
 
 

@@ -128,6 +128,8 @@ struct PostmixParams {
   int P, R;            // positions and rows per tile
   int n_ct;            // channel tiles
   int stacked;         // bwd, nh = 64, pe block = one whole chunk: stacked head mix (below)
+  const int32_t* pos;  // per-row positions (pos0 is added), or null: row s sits at pos0 + s
+  int gs;              // heads per group of the head mix (nh: one [nh, nh] matrix)
 };
 
 struct Tile {
@@ -208,17 +210,22 @@ __device__ __forceinline__ bool group_wait(uint32_t bar, uint32_t parity, volati
   return *slot != 0;
 }
 
-// cos/sin of a = pos * f_i for the P positions of a tile, i < half.
+// cos/sin of a = pos * f_i for the P positions of the tile starting at row
+// s0, i < half. The position of row s is pos0 + s, or pos0 + pos[s] when a
+// positions array is given (rows past sq, which are never stored, take pos0).
 // The angle is reduced exactly in 64-bit fixed point: F[i] = f_i / (2 pi) * 2^64,
-// pos * F[i] mod 2^64 is the fractional turn count; its top 32 bits give a
-// turn in [-1/2, 1/2) that sincospif evaluates.
-__device__ __forceinline__ void fill_rot_table(float2* tab, const uint64_t* F, int64_t pos_first,
-                                               int P, int half, int tid, int nthr) {
-  const int n = P * half;
+// pos * F[i] mod 2^64 is the fractional turn count (two's complement, so a
+// negative position works too); its top 32 bits give a turn in [-1/2, 1/2)
+// that sincospif evaluates.
+__device__ __forceinline__ void fill_rot_table(float2* tab, const uint64_t* F, const PostmixParams& p,
+                                               int64_t s0, int half, int tid, int nthr) {
+  const int n = p.P * half;
   for (int k = tid; k < n; k += nthr) {
     const int pl = k / half;
     const int i = k - pl * half;
-    const uint64_t turns = static_cast<uint64_t>(pos_first + pl) * F[i];
+    const int64_t s = s0 + pl;
+    const int64_t rel = p.pos ? (s < p.sq ? static_cast<int64_t>(__ldg(p.pos + s)) : 0) : s;
+    const uint64_t turns = static_cast<uint64_t>(p.pos0 + rel) * F[i];
     const int32_t ti = static_cast<int32_t>(turns >> 32);
     const float tf = static_cast<float>(ti) * 2.3283064365386963e-10f;  // 2^-32
     float sn, cs;
@@ -363,7 +370,8 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
       ptx::st_shared_v4(base + C::kOffXlo + o, 0u, 0u, 0u, 0u);
   if (threadIdx.x < half) F[threadIdx.x] = p.F[threadIdx.x];
   // M staged in the (still idle) input ring for the A build below, row stride
-  // nh + 1; four independent loads in flight per thread
+  // nh + 1; four independent loads in flight per thread. A grouped mix
+  // (p.M = [nh/gs, gs, gs]) is expanded to its block-diagonal [nh, nh] form.
   float* Ms = reinterpret_cast<float*>(gbase + C::kOffStage);
   {
     const int nn = p.nh * p.nh;
@@ -372,7 +380,10 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int k = k0 + u * blockDim.x;
-        v[u] = k < nn ? __ldg(p.M + k) : 0.f;
+        const int g = k / p.nh, h = k - (k / p.nh) * p.nh;
+        const int b0 = (g / p.gs) * p.gs;  // first head of g's group
+        const bool in = k < nn && h >= b0 && h < b0 + p.gs;
+        v[u] = in ? __ldg(p.M + static_cast<int64_t>(b0) * p.gs + (g - b0) * p.gs + (h - b0)) : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -618,7 +629,7 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
       const Tile x = decode_tile<BWD>(p, t);
       const int pcol = p.nope - x.c0;  // tile-relative column of the first pe channel
       if (x.has_pe) {
-        fill_rot_table(tab, F, p.pos0 + x.s0, p.P, half, e, 128);
+        fill_rot_table(tab, F, p, x.s0, half, e, 128);
         ptx::named_bar_sync(1, 128);
       }
       const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc) * acc_cols;
@@ -884,7 +895,7 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
         if (!group_wait(bar_x_empty, static_cast<uint32_t>((npe & 1) ^ 1), abort_flag,
                         (kRoleTransform << 8) | kBarXEmpty, xr == 0, slot_xf_empty, 2))
           break;
-        fill_rot_table(tab, F, p.pos0 + x.s0, p.P, half, xr, 128);
+        fill_rot_table(tab, F, p, x.s0, half, xr, 128);
         ptx::named_bar_sync(2, 128);
         if (xr < p.R) {
           const int kpe = (p.nope - x.c0) / kChunkCols;
@@ -962,22 +973,27 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
   }
 }
 
-// dM[idx] = sum over the CTA partials ws[c][idx] in a fixed order: thread row ty
-// sums c = ty, ty+8, ... in fp64, then row 0 adds the 8 row sums in order.
+// dM[o] = sum over the CTA partials ws[c][src(o)] in a fixed order: thread row
+// ty sums c = ty, ty+8, ... in fp64, then row 0 adds the 8 row sums in order.
+// The partials are [nh, nh]; a grouped mix keeps only its diagonal blocks:
+// output o = (k, i, j) of [nh/gs, gs, gs] reads entry (k gs + i, k gs + j).
 constexpr int kReduceRows = 8;
 
 __global__ void __launch_bounds__(32 * kReduceRows)
-    dm_reduce_kernel(const float* __restrict__ ws, float* __restrict__ dM, int nparts, int nn) {
+    dm_reduce_kernel(const float* __restrict__ ws, float* __restrict__ dM, int nparts, int nh, int gs) {
   __shared__ double part[kReduceRows][32];
   ptx::griddep_wait();  // launched early (programmatic dependent launch): wait for the partials
+  const int nn = nh * nh, n_out = nh * gs;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int idx = blockIdx.x * 32 + tx;
+  const int k = idx / (gs * gs), rem = idx - k * gs * gs;
+  const int src = (k * gs + rem / gs) * nh + k * gs + rem % gs;
   double s = 0.0;
-  if (idx < nn)
-    for (int c = ty; c < nparts; c += kReduceRows) s += static_cast<double>(ws[static_cast<int64_t>(c) * nn + idx]);
+  if (idx < n_out)
+    for (int c = ty; c < nparts; c += kReduceRows) s += static_cast<double>(ws[static_cast<int64_t>(c) * nn + src]);
   part[ty][tx] = s;
   __syncthreads();
-  if (ty == 0 && idx < nn) {
+  if (ty == 0 && idx < n_out) {
     double t = 0.0;
     for (int k = 0; k < kReduceRows; ++k) t += part[k][tx];
     dM[idx] = static_cast<float>(t);
@@ -1085,17 +1101,29 @@ static int64_t bwd_grid(const Shape& s, int sms) { return s.n_tiles < sms ? s.n_
 
 using namespace invrope;
 
-extern "C" int invrope_postmix_fwd(const void* O, const float* M, void* Y, int64_t sq, int nh, int nope, int pe,
-                                   int64_t pos0, double theta, struct CUstream_st* stream) {
+// Arguments shared by both directions beyond the shape: group size and the
+// optional positions array (validated here; pointers checked by the callers).
+static int check_mix_args(int nh, int gs, const int32_t* positions, int64_t pos0, double theta) {
+  if (gs < 1 || gs > nh || nh % gs != 0) return INVROPE_ERR_INVALID_ARG;
+  if (pos0 < 0 || !valid_theta(theta)) return INVROPE_ERR_INVALID_ARG;
+  if (positions && !aligned(positions, 4)) return INVROPE_ERR_INVALID_ARG;
+  return INVROPE_OK;
+}
+
+extern "C" int invrope_postmix_fwd_ex(const void* O, const float* M, void* Y, int64_t sq, int nh, int gs,
+                                      int nope, int pe, const int32_t* positions, int64_t pos0, double theta,
+                                      struct CUstream_st* stream) {
   Shape s;
   int st = check_shape(sq, nh, nope, pe, KCfg<false>::NC, &s);
   if (st != INVROPE_OK) return st;
-  if (pos0 < 0 || !valid_theta(theta)) return INVROPE_ERR_INVALID_ARG;
+  if ((st = check_mix_args(nh, gs, positions, pos0, theta)) != INVROPE_OK) return st;
   if (sq == 0) return INVROPE_OK;
   if (!O || !M || !Y || !aligned(O, 16) || !aligned(Y, 16) || !aligned(M, 4)) return INVROPE_ERR_INVALID_ARG;
   const size_t tbytes = static_cast<size_t>(sq) * nh * (nope + pe) * 2;
-  const size_t mbytes = static_cast<size_t>(nh) * nh * 4;
-  if (overlaps(Y, tbytes, O, tbytes) || overlaps(Y, tbytes, M, mbytes)) return INVROPE_ERR_INVALID_ARG;
+  const size_t mbytes = static_cast<size_t>(nh) * gs * 4;
+  const size_t pbytes = positions ? static_cast<size_t>(sq) * 4 : 0;
+  if (overlaps(Y, tbytes, O, tbytes) || overlaps(Y, tbytes, M, mbytes) || overlaps(Y, tbytes, positions, pbytes))
+    return INVROPE_ERR_INVALID_ARG;
   DeviceInfo dev;
   if ((st = current_device(&dev)) != INVROPE_OK) return st;
   if ((st = ensure_smem_attr<false>(dev.device)) != INVROPE_OK) return st;
@@ -1119,11 +1147,18 @@ extern "C" int invrope_postmix_fwd(const void* O, const float* M, void* Y, int64
   p.P = s.P;
   p.R = s.R;
   p.n_ct = s.n_ct;
+  p.pos = positions;
+  p.gs = gs;
   fill_freq(p.F, pe, theta);
   const int64_t grid = s.n_tiles < dev.sms ? s.n_tiles : dev.sms;
   postmix_kernel<false><<<static_cast<unsigned>(grid), KCfg<false>::kThreads, KCfg<false>::kSmemAlloc,
                           reinterpret_cast<cudaStream_t>(stream)>>>(p);
   return check_launch();
+}
+
+extern "C" int invrope_postmix_fwd(const void* O, const float* M, void* Y, int64_t sq, int nh, int nope, int pe,
+                                   int64_t pos0, double theta, struct CUstream_st* stream) {
+  return invrope_postmix_fwd_ex(O, M, Y, sq, nh, nh, nope, pe, nullptr, pos0, theta, stream);
 }
 
 extern "C" size_t invrope_postmix_bwd_workspace_bytes(int64_t sq, int nh, int nope, int pe) {
@@ -1135,31 +1170,36 @@ extern "C" size_t invrope_postmix_bwd_workspace_bytes(int64_t sq, int nh, int no
   return static_cast<size_t>(grid) * nh * nh * sizeof(float);
 }
 
-extern "C" int invrope_postmix_bwd(const void* dY, const void* O, const float* M, void* dO, float* dM,
-                                   void* workspace, size_t workspace_bytes, int64_t sq, int nh, int nope, int pe,
-                                   int64_t pos0, double theta, struct CUstream_st* stream) {
+extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float* M, void* dO, float* dM,
+                                      void* workspace, size_t workspace_bytes, int64_t sq, int nh, int gs,
+                                      int nope, int pe, const int32_t* positions, int64_t pos0, double theta,
+                                      struct CUstream_st* stream) {
   Shape s;
   int st = check_shape(sq, nh, nope, pe, KCfg<true>::NC, &s);
   if (st != INVROPE_OK) return st;
-  if (pos0 < 0 || !valid_theta(theta)) return INVROPE_ERR_INVALID_ARG;
+  if ((st = check_mix_args(nh, gs, positions, pos0, theta)) != INVROPE_OK) return st;
   if (!M || !dM || !aligned(M, 4) || !aligned(dM, 4)) return INVROPE_ERR_INVALID_ARG;
   if (sq > 0 && (!dY || !O || !dO || !aligned(dY, 16) || !aligned(O, 16) || !aligned(dO, 16)))
     return INVROPE_ERR_INVALID_ARG;
   const size_t tbytes = static_cast<size_t>(sq) * nh * (nope + pe) * 2;
-  const size_t mbytes = static_cast<size_t>(nh) * nh * 4;
+  const size_t mbytes = static_cast<size_t>(nh) * gs * 4;
+  const size_t pbytes = positions ? static_cast<size_t>(sq) * 4 : 0;
   DeviceInfo dev;
   if ((st = current_device(&dev)) != INVROPE_OK) return st;
   const int64_t grid = sq == 0 ? 0 : bwd_grid(s, dev.sms);
   const size_t need = static_cast<size_t>(grid == 0 ? 1 : grid) * nh * nh * sizeof(float);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return INVROPE_ERR_WORKSPACE;
-  if (overlaps(dO, tbytes, dY, tbytes) || overlaps(dO, tbytes, O, tbytes) || overlaps(dO, tbytes, M, mbytes) ||
-      overlaps(dM, mbytes, dY, tbytes) || overlaps(dM, mbytes, O, tbytes) || overlaps(dM, mbytes, M, mbytes) ||
-      overlaps(dM, mbytes, dO, tbytes) || overlaps(workspace, need, dY, tbytes) ||
-      overlaps(workspace, need, O, tbytes) || overlaps(workspace, need, M, mbytes) ||
-      overlaps(workspace, need, dO, tbytes) || overlaps(workspace, need, dM, mbytes))
-    return INVROPE_ERR_INVALID_ARG;
+  const void* outs[3] = {dO, dM, workspace};
+  const size_t out_bytes[3] = {tbytes, mbytes, need};
+  const void* ins[4] = {dY, O, M, positions};
+  const size_t in_bytes[4] = {tbytes, tbytes, mbytes, pbytes};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = 0; j < 4; ++j)
+      if (overlaps(outs[i], out_bytes[i], ins[j], in_bytes[j])) return INVROPE_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 3; ++j)
+      if (overlaps(outs[i], out_bytes[i], outs[j], out_bytes[j])) return INVROPE_ERR_INVALID_ARG;
+  }
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  const int nn = nh * nh;
   if (grid > 0) {
     if ((st = ensure_smem_attr<true>(dev.device)) != INVROPE_OK) return st;
     PostmixParams p;
@@ -1183,6 +1223,8 @@ extern "C" int invrope_postmix_bwd(const void* dY, const void* O, const float* M
     p.n_ct = s.n_ct;
     // stacked head mix: two positions of 64 heads per tile, pe block = one chunk
     p.stacked = (nh == 64 && pe == kChunkCols && nope % kChunkCols == 0) ? 1 : 0;
+    p.pos = positions;
+    p.gs = gs;
     fill_freq(p.F, pe, theta);
     postmix_kernel<true><<<static_cast<unsigned>(grid), KCfg<true>::kThreads, KCfg<true>::kSmemAlloc, cs>>>(p);
     if ((st = check_launch()) != INVROPE_OK) return st;
@@ -1192,7 +1234,7 @@ extern "C" int invrope_postmix_bwd(const void* dY, const void* O, const float* M
   // for the main kernel's partials. The main kernel does not signal early:
   // reduction blocks that start early crowd onto the first SMs to free up.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((nn + 31) / 32));
+  cfg.gridDim = dim3(static_cast<unsigned>((nh * gs + 31) / 32));
   cfg.blockDim = dim3(32 * kReduceRows);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = cs;
@@ -1202,9 +1244,16 @@ extern "C" int invrope_postmix_bwd(const void* dY, const void* O, const float* M
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const cudaError_t err = cudaLaunchKernelEx(&cfg, dm_reduce_kernel, static_cast<const float*>(workspace), dM,
-                                             static_cast<int>(grid), nn);
+                                             static_cast<int>(grid), nh, gs);
   if (err != cudaSuccess) return cuda_fail(err);
   return check_launch();
+}
+
+extern "C" int invrope_postmix_bwd(const void* dY, const void* O, const float* M, void* dO, float* dM,
+                                   void* workspace, size_t workspace_bytes, int64_t sq, int nh, int nope, int pe,
+                                   int64_t pos0, double theta, struct CUstream_st* stream) {
+  return invrope_postmix_bwd_ex(dY, O, M, dO, dM, workspace, workspace_bytes, sq, nh, nh, nope, pe, nullptr, pos0,
+                                theta, stream);
 }
 
 extern "C" int invrope_watchdog_selftest(int64_t limit_us, int* fault) {

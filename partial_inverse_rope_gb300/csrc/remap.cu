@@ -10,6 +10,7 @@
 // element range [b*sq*topk, (b+1)*sq*topk), so a thread block that walks a
 // chunk of the flat array finds its batch with one division per chunk and
 // at most one boundary inside it. 16-byte vectors when the layout allows.
+// int32 and int64 tables (the int64 one for callers that index past 2^31).
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -23,29 +24,44 @@ constexpr int kThreads = 256;
 constexpr int kPer = 8;                         // vectors per thread per chunk
 constexpr int kChunk = kThreads * kPer;         // vectors per chunk
 
-__device__ __forceinline__ int32_t remap1(int32_t v, uint32_t off) {
-  return v < 0 ? v : static_cast<int32_t>(static_cast<uint32_t>(v) + off);
+// Entry types: int32 (offset added mod 2^32) and int64 (mod 2^64).
+__device__ __forceinline__ int32_t remap1(int32_t v, uint64_t off) {
+  return v < 0 ? v : static_cast<int32_t>(static_cast<uint32_t>(v) + static_cast<uint32_t>(off));
+}
+__device__ __forceinline__ long long remap1(long long v, uint64_t off) {
+  return v < 0 ? v : static_cast<long long>(static_cast<uint64_t>(v) + off);
 }
 
 __device__ __forceinline__ int4 load_vec(const int4* p) { return __ldcs(p); }
 __device__ __forceinline__ int load_vec(const int* p) { return __ldcs(p); }
+__device__ __forceinline__ longlong2 load_vec(const longlong2* p) { return __ldcs(p); }
+__device__ __forceinline__ long long load_vec(const long long* p) { return __ldcs(p); }
 __device__ __forceinline__ void store_vec(int4* p, int4 v) { __stcs(p, v); }
 __device__ __forceinline__ void store_vec(int* p, int v) { __stcs(p, v); }
+__device__ __forceinline__ void store_vec(longlong2* p, longlong2 v) { __stcs(p, v); }
+__device__ __forceinline__ void store_vec(long long* p, long long v) { __stcs(p, v); }
 
-__device__ __forceinline__ int4 remap_vec(int4 v, uint32_t off) {
+__device__ __forceinline__ int4 remap_vec(int4 v, uint64_t off) {
   v.x = remap1(v.x, off);
   v.y = remap1(v.y, off);
   v.z = remap1(v.z, off);
   v.w = remap1(v.w, off);
   return v;
 }
-__device__ __forceinline__ int remap_vec(int v, uint32_t off) { return remap1(v, off); }
+__device__ __forceinline__ int remap_vec(int v, uint64_t off) { return remap1(v, off); }
+__device__ __forceinline__ longlong2 remap_vec(longlong2 v, uint64_t off) {
+  v.x = remap1(v.x, off);
+  v.y = remap1(v.y, off);
+  return v;
+}
+__device__ __forceinline__ long long remap_vec(long long v, uint64_t off) { return remap1(v, off); }
 
-// V = int4 (4 entries) or int (1 entry). seg = entries of one batch in units of V.
+// V = a 16-byte vector (int4: 4 int32 entries, longlong2: 2 int64 entries) or
+// one entry. seg = entries of one batch in units of V.
 // kOneBoundary: seg >= kChunk, so a chunk crosses at most one batch boundary.
 template <typename V, bool kOneBoundary>
 __global__ void __launch_bounds__(kThreads) kv_remap_kernel(const V* in, V* out, int64_t n, int64_t seg,
-                                                            uint32_t seqlen_kv) {
+                                                            uint64_t seqlen_kv) {
   const int64_t nchunks = (n + kChunk - 1) / kChunk;
   for (int64_t ch = blockIdx.x; ch < nchunks; ch += gridDim.x) {
     const int64_t v0 = ch * kChunk;
@@ -62,15 +78,14 @@ __global__ void __launch_bounds__(kThreads) kv_remap_kernel(const V* in, V* out,
       const int64_t v = v0 + k * kThreads + threadIdx.x;
       if (v < n) {
         const int64_t b = kOneBoundary ? b0 + (v >= boundary ? 1 : 0) : v / seg;
-        const uint32_t off = static_cast<uint32_t>(static_cast<uint64_t>(b) * seqlen_kv);
-        store_vec(out + v, remap_vec(x[k], off));
+        store_vec(out + v, remap_vec(x[k], static_cast<uint64_t>(b) * seqlen_kv));
       }
     }
   }
 }
 
 template <typename V>
-int launch(const void* in, void* out, int64_t n, int64_t seg, uint32_t skv, int sms, cudaStream_t s) {
+int launch(const void* in, void* out, int64_t n, int64_t seg, uint64_t skv, int sms, cudaStream_t s) {
   const int64_t nchunks = (n + kChunk - 1) / kChunk;
   const int64_t grid = nchunks < static_cast<int64_t>(sms) * 8 ? nchunks : static_cast<int64_t>(sms) * 8;
   if (seg >= kChunk)
@@ -82,6 +97,19 @@ int launch(const void* in, void* out, int64_t n, int64_t seg, uint32_t skv, int 
   return check_launch();
 }
 
+// Argument checks common to both entry types; returns the entry count in *n.
+int check_remap(const void* idx, const void* out, int64_t rows, int topk, int64_t sq, int64_t seqlen_kv,
+                size_t esize, int64_t* n) {
+  if (rows < 0 || topk < 0 || sq < 1 || seqlen_kv < 0) return INVROPE_ERR_INVALID_ARG;
+  if (rows % sq != 0) return INVROPE_ERR_INVALID_ARG;
+  *n = rows * static_cast<int64_t>(topk);
+  if (*n == 0) return INVROPE_OK;
+  if (!idx || !out || !aligned(idx, esize) || !aligned(out, esize)) return INVROPE_ERR_INVALID_ARG;
+  const size_t bytes = static_cast<size_t>(*n) * esize;
+  if (idx != out && overlaps(idx, bytes, out, bytes)) return INVROPE_ERR_INVALID_ARG;
+  return INVROPE_OK;
+}
+
 }  // namespace
 }  // namespace invrope
 
@@ -89,21 +117,38 @@ using namespace invrope;
 
 extern "C" int kv_idx_local_to_global(const int32_t* idx, int32_t* out, int64_t rows, int topk, int64_t sq,
                                       int64_t seqlen_kv, struct CUstream_st* stream) {
-  if (rows < 0 || topk < 0 || sq < 1 || seqlen_kv < 0) return INVROPE_ERR_INVALID_ARG;
-  if (rows % sq != 0) return INVROPE_ERR_INVALID_ARG;
-  const int64_t nb = rows / sq;
-  if (nb > 0 && nb * seqlen_kv > (int64_t(1) << 31)) return INVROPE_ERR_INVALID_ARG;
-  const int64_t n = rows * static_cast<int64_t>(topk);
-  if (n == 0) return INVROPE_OK;
-  if (!idx || !out || !aligned(idx, 4) || !aligned(out, 4)) return INVROPE_ERR_INVALID_ARG;
-  if (idx != out && overlaps(idx, n * 4, out, n * 4)) return INVROPE_ERR_INVALID_ARG;
-  DeviceInfo dev;
-  int st = current_device(&dev);
+  int64_t n = 0;
+  int st = check_remap(idx, out, rows, topk, sq, seqlen_kv, 4, &n);
   if (st != INVROPE_OK) return st;
+  const int64_t nb = rows / sq;
+  if (nb > 0 && seqlen_kv > (int64_t(1) << 31) / nb) return INVROPE_ERR_INVALID_ARG;  // b*seqlen_kv <= 2^31
+  if (n == 0) return INVROPE_OK;
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != INVROPE_OK) return st;
   const int64_t seg = sq * topk;  // entries per batch
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const uint32_t skv = static_cast<uint32_t>(seqlen_kv);
+  const uint64_t skv = static_cast<uint64_t>(seqlen_kv);
   if (aligned(idx, 16) && aligned(out, 16) && seg % 4 == 0)
     return launch<int4>(idx, out, n / 4, seg / 4, skv, dev.sms, s);
   return launch<int>(idx, out, n, seg, skv, dev.sms, s);
+}
+
+extern "C" int kv_idx_local_to_global_i64(const int64_t* idx, int64_t* out, int64_t rows, int topk, int64_t sq,
+                                          int64_t seqlen_kv, struct CUstream_st* stream) {
+  int64_t n = 0;
+  int st = check_remap(idx, out, rows, topk, sq, seqlen_kv, 8, &n);
+  if (st != INVROPE_OK) return st;
+  const int64_t nb = rows / sq;
+  // b * seqlen_kv <= 2^63: every in-range index maps into int64
+  if (nb > 0 && static_cast<uint64_t>(seqlen_kv) > (uint64_t(1) << 63) / static_cast<uint64_t>(nb))
+    return INVROPE_ERR_INVALID_ARG;
+  if (n == 0) return INVROPE_OK;
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != INVROPE_OK) return st;
+  const int64_t seg = sq * topk;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint64_t skv = static_cast<uint64_t>(seqlen_kv);
+  if (aligned(idx, 16) && aligned(out, 16) && seg % 2 == 0)
+    return launch<longlong2>(idx, out, n / 2, seg / 2, skv, dev.sms, s);
+  return launch<long long>(idx, out, n, seg, skv, dev.sms, s);
 }

@@ -98,6 +98,19 @@ def postmix_M(nh: int, seed: int, device="cpu") -> torch.Tensor:
     return torch.eye(nh, device=device, dtype=torch.float32) + 0.02 * z
 
 
+def postmix_Mg(ng: int, gs: int, seed: int, device="cpu") -> torch.Tensor:
+    """Grouped mix ``[ng, gs, gs]``: ``I + 0.02 * N(0, 1)`` per group, fp32."""
+    g = _gen(seed, device)
+    z = torch.randn(ng, gs, gs, generator=g, device=device, dtype=torch.float32)
+    return torch.eye(gs, device=device, dtype=torch.float32)[None] + 0.02 * z
+
+
+def random_positions(sq: int, seed: int, low: int, high: int, device="cpu") -> torch.Tensor:
+    """int32 ``[sq]`` positions drawn uniformly from ``[low, high)``."""
+    g = _gen(seed, device)
+    return torch.randint(low, high, (sq,), generator=g, device=device, dtype=torch.int32)
+
+
 def postmix_inputs(cfg: PostmixConfig, device="cpu", layer: int = 0):
     """``(O, dY, M)`` for one layer of ``cfg``."""
     shape = (cfg.sq, cfg.nh, cfg.d)

@@ -38,7 +38,8 @@ def test_header_declares_the_expected_entry_points():
     assert _declared_functions() == sorted([
         "invrope_last_cuda_error", "invrope_postmix_bwd", "invrope_postmix_bwd_workspace_bytes",
         "invrope_postmix_bwd_noalloc", "invrope_postmix_fwd", "invrope_status_string",
-        "invrope_take_device_fault", "invrope_watchdog_selftest", "kv_idx_local_to_global"])
+        "invrope_take_device_fault", "invrope_watchdog_selftest", "kv_idx_local_to_global",
+        "invrope_postmix_fwd_ex", "invrope_postmix_bwd_ex", "kv_idx_local_to_global_i64"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -105,6 +106,29 @@ def test_bwd_rejects_bad_arguments_on_the_host(lib):
                                    8, 200, 448, 64, 0, 1e4, None) == UNSUPPORTED
 
 
+@pytest.mark.parametrize("nh,gs,positions", [
+    (4, 0, None),        # empty groups
+    (4, 3, None),        # group size does not divide nh
+    (4, 8, None),        # group larger than nh
+    (4, 2, FAKE + 2),    # misaligned positions array
+])
+def test_grouped_and_positions_reject_bad_arguments(lib, nh, gs, positions):
+    assert lib.invrope_postmix_fwd_ex(FAKE, FAKE * 4, FAKE * 2, 8, nh, gs, 48, 16, positions, 0, 1e4,
+                                      None) == INVALID
+    assert lib.invrope_postmix_bwd_ex(FAKE, FAKE * 2, FAKE * 3, FAKE * 4, FAKE * 5, FAKE * 6, 1 << 20,
+                                      8, nh, gs, 48, 16, positions, 0, 1e4, None) == INVALID
+
+
+def test_fwd_ex_rejects_output_over_positions(lib):
+    # Y = [8, 4, 64] bf16 (4 KB) starting 64 bytes before the positions array
+    assert lib.invrope_postmix_fwd_ex(FAKE, FAKE * 8, FAKE * 2, 8, 4, 2, 48, 16, FAKE * 2 + 64, 0, 1e4,
+                                      None) == INVALID
+
+
+def test_fwd_ex_with_no_rows_is_a_no_op(lib):
+    assert lib.invrope_postmix_fwd_ex(None, None, None, 0, 4, 2, 48, 16, None, 0, 1e4, None) == OK
+
+
 def test_workspace_query_is_zero_for_invalid_shapes(lib):
     assert lib.invrope_postmix_bwd_workspace_bytes(8, 0, 448, 64) == 0
     assert lib.invrope_postmix_bwd_workspace_bytes(8, 4, 448, 63) == 0
@@ -120,6 +144,22 @@ def test_workspace_query_is_zero_for_invalid_shapes(lib):
 ])
 def test_remap_rejects_bad_arguments(lib, rows, topk, sq, skv, want):
     assert lib.kv_idx_local_to_global(FAKE, FAKE * 4, rows, topk, sq, skv, None) == want
+
+
+@pytest.mark.parametrize("rows,topk,sq,skv,want", [
+    (10, 4, 3, 100, INVALID),              # rows not a multiple of sq
+    (8, 4, 0, 100, INVALID),               # sq = 0
+    (8, 4, 4, -1, INVALID),                # negative seqlen_kv
+    (8, 4, 2, 2**62, INVALID),             # 4 batches * 2^62 > 2^63
+])
+def test_remap_i64_rejects_bad_arguments(lib, rows, topk, sq, skv, want):
+    assert lib.kv_idx_local_to_global_i64(FAKE, FAKE * 4, rows, topk, sq, skv, None) == want
+
+
+def test_remap_i64_rejects_misaligned_or_overlapping_tables(lib):
+    assert lib.kv_idx_local_to_global_i64(FAKE + 4, FAKE * 4, 8, 4, 4, 100, None) == INVALID
+    assert lib.kv_idx_local_to_global_i64(FAKE, FAKE + 8, 8, 4, 4, 100, None) == INVALID
+    assert lib.kv_idx_local_to_global_i64(None, None, 0, 16, 4, 100, None) == OK
 
 
 def test_remap_empty_table_is_a_no_op(lib):
