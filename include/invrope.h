@@ -33,10 +33,12 @@
  *   - Pointers are DEVICE pointers of the current CUDA device, owned by the
  *     caller. The library allocates no device memory at call time and keeps
  *     no state between calls beyond cached device attributes, loaded kernels
- *     and a 2 KB per-device array of tile counters: the forward hands out
- *     its tiles dynamically (thread blocks claim the next tile from a
- *     counter), and the last thread block of a launch returns its counter
- *     to zero.
+ *     and two small per-device arrays of work counters (2 KB for the
+ *     forward's tiles, 4 KB for the remap's chunks): those kernels hand out
+ *     their work dynamically (thread blocks claim the next tile or chunk from
+ *     a counter), and the last thread block of a launch returns its counter
+ *     to zero. A launch takes one of 256 counters in turn, so at most 256
+ *     such launches may run at once per device.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream). Every call
  *     only enqueues work on `stream` and returns; nothing synchronises.
  *   - Arguments are validated on the host before anything is enqueued; a

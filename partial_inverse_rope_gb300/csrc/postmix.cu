@@ -108,7 +108,7 @@ struct KCfg {
   static constexpr int kSmemAlloc = kSmemBytes + 1024;   // slack to align the base
   static_assert(kSmemAlloc <= 232448, "shared memory budget");
   static_assert(kNumAcc * NC + (BWD ? 128 : 0) <= kACol, "TMEM budget");
-  static_assert(kStages * kStageBytes >= 128 * 128 * 4, "dM partial reduction reuses the input ring");
+  static_assert(kStages * kStageBytes >= 128 * 129 * 4, "dM partial reduction reuses the input ring");
   static_assert(kOutInflight >= 1, "at least one store in flight");
 };
 
@@ -811,8 +811,10 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
       // input ring is free once every MMA has completed.
       if (group_wait(bar_d2, 0, abort_flag, (kRoleEpilogue << 8) | kBarD2, e == 0, slot_d2, 1)) {
         ptx::tc_fence_after();
-        // red[h * R + r] = D2[r][pl*nh + h]: consecutive rows -> consecutive words
+        // red[h * (R + 1) + r] = D2[r][pl*nh + h]: consecutive rows -> consecutive
+        // words; the odd row stride keeps the transposed reads below conflict-free
         float* red = reinterpret_cast<float*>(gbase + C::kOffStage);
+        const int rs = p.R + 1;
         const int lo = pl * p.nh;
         for (int j0 = 0; j0 < 128; j0 += 32) {
           uint32_t v[32];
@@ -822,16 +824,17 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
               const int j = j0 + jj;
-              if (j >= lo && j < lo + p.nh) red[(j - lo) * p.R + r] = __uint_as_float(v[jj]);
+              if (j >= lo && j < lo + p.nh) red[(j - lo) * rs + r] = __uint_as_float(v[jj]);
             }
           }
         }
         ptx::named_bar_sync(1, 128);
         const int nn = p.nh * p.nh;
+        // consecutive threads take consecutive h: coalesced partial rows
         for (int idx = e; idx < nn; idx += 128) {
-          const int h = idx / p.nh, g = idx - h * p.nh;
+          const int g = idx / p.nh, h = idx - g * p.nh;
           float s = 0.f;
-          for (int q = 0; q < p.P; ++q) s += red[h * p.R + q * p.nh + g];
+          for (int q = 0; q < p.P; ++q) s += red[h * rs + q * p.nh + g];
           p.ws[static_cast<int64_t>(blockIdx.x) * nn + g * p.nh + h] = s;
         }
       }
@@ -989,8 +992,10 @@ __global__ void __launch_bounds__(32 * kReduceRows)
   const int k = idx / (gs * gs), rem = idx - k * gs * gs;
   const int src = (k * gs + rem / gs) * nh + k * gs + rem % gs;
   double s = 0.0;
-  if (idx < n_out)
+  if (idx < n_out) {
+#pragma unroll 4
     for (int c = ty; c < nparts; c += kReduceRows) s += static_cast<double>(ws[static_cast<int64_t>(c) * nn + src]);
+  }
   part[ty][tx] = s;
   __syncthreads();
   if (ty == 0 && idx < n_out) {

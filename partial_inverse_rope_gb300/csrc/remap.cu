@@ -10,14 +10,24 @@
 // element range [b*sq*topk, (b+1)*sq*topk), so a thread block that walks a
 // chunk of the flat array finds its batch with one division per chunk and
 // at most one boundary inside it. 16-byte vectors when the layout allows.
+// Chunks are handed out dynamically (a per-launch counter): SMs differ in the
+// memory bandwidth they get, and a fixed split would wait on the slowest.
 // int32 and int64 tables (the int64 one for callers that index past 2^31).
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "common.h"
 
 namespace invrope {
+
+// Dynamic chunk scheduling: one {next chunk, finished blocks} pair per launch
+// slot; a launch takes slot (launch sequence number mod kRemapSlots) and its
+// last block returns the pair to zero.
+constexpr int kRemapSlots = 256;
+__device__ unsigned long long g_remap_sched[kRemapSlots][2];
+
 namespace {
 
 constexpr int kThreads = 256;
@@ -61,9 +71,12 @@ __device__ __forceinline__ long long remap_vec(long long v, uint64_t off) { retu
 // kOneBoundary: seg >= kChunk, so a chunk crosses at most one batch boundary.
 template <typename V, bool kOneBoundary>
 __global__ void __launch_bounds__(kThreads) kv_remap_kernel(const V* in, V* out, int64_t n, int64_t seg,
-                                                            uint64_t seqlen_kv) {
+                                                            uint64_t seqlen_kv, unsigned long long* sched) {
+  __shared__ int64_t next_chunk;
   const int64_t nchunks = (n + kChunk - 1) / kChunk;
-  for (int64_t ch = blockIdx.x; ch < nchunks; ch += gridDim.x) {
+  // first chunk = block index; each later one is claimed while the current one streams
+  for (int64_t ch = blockIdx.x; ch < nchunks;) {
+    if (threadIdx.x == 0) next_chunk = static_cast<int64_t>(gridDim.x + atomicAdd(sched, 1ull));
     const int64_t v0 = ch * kChunk;
     const int64_t b0 = v0 / seg;
     const int64_t boundary = (b0 + 1) * seg;
@@ -81,19 +94,52 @@ __global__ void __launch_bounds__(kThreads) kv_remap_kernel(const V* in, V* out,
         store_vec(out + v, remap_vec(x[k], static_cast<uint64_t>(b) * seqlen_kv));
       }
     }
+    __syncthreads();  // next_chunk is visible
+    ch = next_chunk;
+    __syncthreads();  // and read by all before thread 0 claims again
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(sched + 1, 1ull) == gridDim.x - 1) {  // last block: reset the slot
+      sched[0] = 0;
+      sched[1] = 0;
+      __threadfence();
+    }
   }
 }
 
+// This launch's counter pair on device `device` (address looked up once per device).
+int remap_slot(int device, unsigned long long** out) {
+  static std::mutex mu;
+  static unsigned long long* base[64] = {};
+  static unsigned int seq[64] = {};
+  if (device < 0 || device >= 64) return INVROPE_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!base[device]) {
+    void* ptr = nullptr;
+    const cudaError_t err = cudaGetSymbolAddress(&ptr, g_remap_sched);
+    if (err != cudaSuccess) return cuda_fail(err);
+    base[device] = static_cast<unsigned long long*>(ptr);
+  }
+  *out = base[device] + 2 * (seq[device]++ % kRemapSlots);
+  return INVROPE_OK;
+}
+
 template <typename V>
-int launch(const void* in, void* out, int64_t n, int64_t seg, uint64_t skv, int sms, cudaStream_t s) {
+int launch(const void* in, void* out, int64_t n, int64_t seg, uint64_t skv, const DeviceInfo& dev,
+           cudaStream_t s) {
+  unsigned long long* sched = nullptr;
+  const int st = remap_slot(dev.device, &sched);
+  if (st != INVROPE_OK) return st;
   const int64_t nchunks = (n + kChunk - 1) / kChunk;
-  const int64_t grid = nchunks < static_cast<int64_t>(sms) * 8 ? nchunks : static_cast<int64_t>(sms) * 8;
+  const int64_t slots = static_cast<int64_t>(dev.sms) * 8;
+  const int64_t grid = nchunks < slots ? nchunks : slots;
   if (seg >= kChunk)
     kv_remap_kernel<V, true><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(
-        static_cast<const V*>(in), static_cast<V*>(out), n, seg, skv);
+        static_cast<const V*>(in), static_cast<V*>(out), n, seg, skv, sched);
   else
     kv_remap_kernel<V, false><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(
-        static_cast<const V*>(in), static_cast<V*>(out), n, seg, skv);
+        static_cast<const V*>(in), static_cast<V*>(out), n, seg, skv, sched);
   return check_launch();
 }
 
@@ -129,8 +175,8 @@ extern "C" int kv_idx_local_to_global(const int32_t* idx, int32_t* out, int64_t 
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const uint64_t skv = static_cast<uint64_t>(seqlen_kv);
   if (aligned(idx, 16) && aligned(out, 16) && seg % 4 == 0)
-    return launch<int4>(idx, out, n / 4, seg / 4, skv, dev.sms, s);
-  return launch<int>(idx, out, n, seg, skv, dev.sms, s);
+    return launch<int4>(idx, out, n / 4, seg / 4, skv, dev, s);
+  return launch<int>(idx, out, n, seg, skv, dev, s);
 }
 
 extern "C" int kv_idx_local_to_global_i64(const int64_t* idx, int64_t* out, int64_t rows, int topk, int64_t sq,
@@ -149,6 +195,6 @@ extern "C" int kv_idx_local_to_global_i64(const int64_t* idx, int64_t* out, int6
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const uint64_t skv = static_cast<uint64_t>(seqlen_kv);
   if (aligned(idx, 16) && aligned(out, 16) && seg % 2 == 0)
-    return launch<longlong2>(idx, out, n / 2, seg / 2, skv, dev.sms, s);
-  return launch<long long>(idx, out, n, seg, skv, dev.sms, s);
+    return launch<longlong2>(idx, out, n / 2, seg / 2, skv, dev, s);
+  return launch<long long>(idx, out, n, seg, skv, dev, s);
 }
