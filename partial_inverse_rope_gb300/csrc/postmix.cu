@@ -82,7 +82,7 @@ struct KCfg {
   static constexpr int kTensorTile = kChunks * kChunkBytes;
   static constexpr int kStageBytes = (BWD ? 2 : 1) * kTensorTile;   // input ring entry
   static constexpr int kStages = 4;                      // input ring
-  static constexpr int kOutBufs = BWD ? 4 : 5;           // output ring of 64-channel chunks
+  static constexpr int kOutBufs = BWD ? 3 : 5;           // output ring of 64-channel chunks
   static constexpr int kOutInflight = kOutBufs - 2;      // TMA stores left reading smem
   static constexpr int kNumAcc = BWD ? 4 : 3;
   // TMEM columns: accumulators, then dM (bwd), then A hi (64) and A lo (64)
@@ -97,8 +97,11 @@ struct KCfg {
   static constexpr int kOffOut = kOffStage + kStages * kStageBytes;
   static constexpr int kOffXlo = kOffOut + kOutBufs * kChunkBytes;
   static constexpr int kXloBytes = BWD ? kChunkBytes : 0;
+  // bwd, stacked mix: fp32 exchange rows between the epilogue warp pairs (64 x 256 B)
+  static constexpr int kOffXch = kOffXlo + kXloBytes;
+  static constexpr int kXchBytes = BWD ? 64 * 256 : 0;
   static constexpr int kTabBytes = kPosPerTileMax * kMaxHalf * 8;
-  static constexpr int kOffTabEpi = kOffXlo + kXloBytes;
+  static constexpr int kOffTabEpi = kOffXch + kXchBytes;
   static constexpr int kOffTabXf = kOffTabEpi + kTabBytes;
   static constexpr int kOffFreq = kOffTabXf + (BWD ? kTabBytes : 0);
   static constexpr int kOffBars = kOffFreq + kMaxHalf * 8;
@@ -644,64 +647,83 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
         const bool pe_chunk = x.has_pe && (pcol >> 6) == k;
         const bool pe_whole = pe_chunk && half == 32;  // the pe block is exactly this chunk
         if (stk) {
-          // Stacked mix: lane h < 64 holds the hi rows of head h, lane 64 + h
-          // its lo rows; D column 64 p + c is channel c of position p, whose
-          // output row is 64 p + h. The lo warps park their terms (bf16) in
-          // the output buffer; the hi warps add them, rotate, round, overwrite.
+          // Stacked mix: lane h < 64 (quads 0, 1) holds the hi rows of head h,
+          // lane 64 + h (quads 2, 3) its lo rows; D column 64 p + c is channel c
+          // of position p, whose output row is 64 p + h. Each warp pair splits
+          // the work by position: the hi warps finish position 0 and hand their
+          // position-1 terms (fp32, exchange rows) to the lo warps, which finish
+          // position 1 and hand over their position-0 terms through the output
+          // buffer as bf16 (a lo term is ~2^-9 of the result, so that rounding
+          // costs ~2^-17 relative).
           const int h = r & 63;
-          if (quad >= 2) {
+          const bool hi = quad < 2;
+          const uint32_t xrow = base + C::kOffXch + static_cast<uint32_t>(h) * 256u;
+          const uint32_t hx = static_cast<uint32_t>(h & 7);  // unit c of a row sits at (c ^ hx) * 16
+          {
+            uint32_t v[64];
+            ptx::tmem_ld_x64(taddr + (hi ? 64 : 0), v);
+            ptx::tmem_ld_wait(v);
+            if (hi) {
 #pragma unroll
-            for (int pp = 0; pp < 2; ++pp) {
-              uint32_t v[64];
-              ptx::tmem_ld_x64(taddr + pp * 64, v);
-              ptx::tmem_ld_wait(v);
+              for (int c = 0; c < 16; ++c)
+                ptx::st_shared_v4(xrow + ((static_cast<uint32_t>(c) ^ hx) << 4), v[4 * c], v[4 * c + 1],
+                                  v[4 * c + 2], v[4 * c + 3]);
+            } else {
 #pragma unroll
               for (int u = 0; u < 8; ++u) {
-                const uint32_t w0 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]));
-                const uint32_t w1 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]));
-                const uint32_t w2 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]));
-                const uint32_t w3 = ptx::pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7]));
-                ptx::st_shared_v4(swz_unit_addr(ob, pp * 64 + h, 8 * u), w0, w1, w2, w3);
+                const uint32_t* w = v + 8 * u;
+                ptx::st_shared_v4(swz_unit_addr(ob, h, 8 * u),
+                                  ptx::pack_bf16x2(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                                  ptx::pack_bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3])),
+                                  ptx::pack_bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5])),
+                                  ptx::pack_bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7])));
               }
             }
           }
-          ptx::named_bar_sync(3, 128);  // the lo terms are in the output buffer
-          if (quad < 2) {
-#pragma unroll 1
-            for (int pp = 0; pp < 2; ++pp) {
-              uint32_t v[64];
-              ptx::tmem_ld_x64(taddr + pp * 64, v);
-              ptx::tmem_ld_wait(v);
-              const int row = pp * 64 + h;
-              float y[64];
+          uint32_t y[64];  // this warp's own position: hi position 0, lo position 1
+          ptx::tmem_ld_x64(taddr + (hi ? 0 : 64), y);
+          ptx::tmem_ld_wait(y);
+          ptx::named_bar_sync(3, 128);  // both halves are parked
+          const int pp = hi ? 0 : 1;
+          const int row = pp * 64 + h;
+          if (hi) {
+            uint32_t l[32];
 #pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                uint32_t l[4];
-                ptx::ld_shared_v4(swz_unit_addr(ob, row, 8 * u), l[0], l[1], l[2], l[3]);
+            for (int u = 0; u < 8; ++u)
+              ptx::ld_shared_v4(swz_unit_addr(ob, h, 8 * u), l[4 * u], l[4 * u + 1], l[4 * u + 2], l[4 * u + 3]);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  y[8 * u + 2 * q] = __uint_as_float(v[8 * u + 2 * q]) + ptx::bf16_lo_f32(l[q]);
-                  y[8 * u + 2 * q + 1] = __uint_as_float(v[8 * u + 2 * q + 1]) + ptx::bf16_hi_f32(l[q]);
-                }
-              }
-              if (pe_chunk) {
-                // the chunk is the whole pe block: pairs (i, 32 + i)
-                const float2* rt = tab + pp * 32;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                  const float2 cs = rt[i];
-                  const float x1 = y[i], x2 = y[32 + i];
-                  y[i] = x1 * cs.x - sgn * x2 * cs.y;
-                  y[32 + i] = x2 * cs.x + sgn * x1 * cs.y;
-                }
-              }
-#pragma unroll
-              for (int u = 0; u < 8; ++u)
-                ptx::st_shared_v4(swz_unit_addr(ob, row, 8 * u), ptx::pack_bf16x2(y[8 * u + 0], y[8 * u + 1]),
-                                  ptx::pack_bf16x2(y[8 * u + 2], y[8 * u + 3]),
-                                  ptx::pack_bf16x2(y[8 * u + 4], y[8 * u + 5]),
-                                  ptx::pack_bf16x2(y[8 * u + 6], y[8 * u + 7]));
+            for (int q = 0; q < 32; ++q) {
+              y[2 * q] = __float_as_uint(__uint_as_float(y[2 * q]) + ptx::bf16_lo_f32(l[q]));
+              y[2 * q + 1] = __float_as_uint(__uint_as_float(y[2 * q + 1]) + ptx::bf16_hi_f32(l[q]));
             }
+          } else {
+            uint32_t f[64];
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+              ptx::ld_shared_v4(xrow + ((static_cast<uint32_t>(c) ^ hx) << 4), f[4 * c], f[4 * c + 1],
+                                f[4 * c + 2], f[4 * c + 3]);
+#pragma unroll
+            for (int k = 0; k < 64; ++k) y[k] = __float_as_uint(__uint_as_float(y[k]) + __uint_as_float(f[k]));
+          }
+          if (pe_chunk) {
+            // the chunk is the whole pe block: pairs (i, 32 + i)
+            const float2* rt = tab + pp * 32;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float2 cs = rt[i];
+              const float x1 = __uint_as_float(y[i]), x2 = __uint_as_float(y[32 + i]);
+              y[i] = __float_as_uint(x1 * cs.x - sgn * x2 * cs.y);
+              y[32 + i] = __float_as_uint(x2 * cs.x + sgn * x1 * cs.y);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint32_t* w = y + 8 * u;
+            ptx::st_shared_v4(swz_unit_addr(ob, row, 8 * u),
+                              ptx::pack_bf16x2(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                              ptx::pack_bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3])),
+                              ptx::pack_bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5])),
+                              ptx::pack_bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7])));
           }
         } else {
           if (!pe_whole) {
@@ -866,7 +888,7 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
           ptx::tma_store_2d(&p.tm_out, out_addr(b), x.c0 + k * kChunkCols, x.row0);
           ptx::bulk_commit();
           // keep kIn stores reading; recycle the buffer of the oldest finished one
-          if (n >= kIn - 1) {
+          if (n + 1u >= static_cast<uint32_t>(kIn)) {
             ptx::bulk_wait_read<kIn - 1>();
             ptx::mbar_arrive(bar_ob_empty(static_cast<int>((n - (kIn - 1)) % OB)));
           }
