@@ -614,9 +614,23 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
       if (BWD && t_begin + i >= t_end) break;
       const int acc = acc_of(i);
       const uint32_t aph = acc_phase(i);
-      if (!group_wait(bar_acc_full(acc), aph, abort_flag, (kRoleEpilogue << 8) | kBarAccFull, e == 0,
-                      slot_epi + (i & 1), 1))
+      if (stk) {
+        // one group barrier for both waits: this tile's accumulator and its output buffer
+        volatile int* slot = slot_epi + (i & 1);
+        if (e == 0) {
+          const int b = static_cast<int>(n % OB);
+          *slot = wait_bar(bar_acc_full(acc), aph, abort_flag, (kRoleEpilogue << 8) | kBarAccFull) &&
+                          wait_bar(bar_ob_empty(b), ((n / OB) & 1u) ^ 1u, abort_flag,
+                                   (kRoleEpilogue << 8) | kBarOut)
+                      ? 1
+                      : 0;
+        }
+        ptx::named_bar_sync(1, 128);
+        if (*slot == 0) break;
+      } else if (!group_wait(bar_acc_full(acc), aph, abort_flag, (kRoleEpilogue << 8) | kBarAccFull, e == 0,
+                             slot_epi + (i & 1), 1)) {
         break;
+      }
       ptx::tc_fence_after();
       const int64_t t = BWD ? t_begin + i : static_cast<int64_t>(acc_tile[acc]);
       if (!BWD && t < 0) {
@@ -638,8 +652,8 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
       const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc) * acc_cols;
       for (int k = 0; k < x.nch; ++k, ++n) {
         const int b = static_cast<int>(n % OB);
-        if (!group_wait(bar_ob_empty(b), ((n / OB) & 1u) ^ 1u, abort_flag,
-                        (kRoleEpilogue << 8) | kBarOut, e == 0, slot_ob + (n & 1), 1)) {
+        if (!stk && !group_wait(bar_ob_empty(b), ((n / OB) & 1u) ^ 1u, abort_flag,
+                                (kRoleEpilogue << 8) | kBarOut, e == 0, slot_ob + (n & 1), 1)) {
           ok = false;
           break;
         }
@@ -659,10 +673,14 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
           const bool hi = quad < 2;
           const uint32_t xrow = base + C::kOffXch + static_cast<uint32_t>(h) * 256u;
           const uint32_t hx = static_cast<uint32_t>(h & 7);  // unit c of a row sits at (c ^ hx) * 16
+          // both halves out of TMEM in one round trip; the accumulator is then free
+          uint32_t v[64], y[64];  // y: this warp's own position (hi: 0, lo: 1)
+          ptx::tmem_ld_x64(taddr + (hi ? 64 : 0), v);
+          ptx::tmem_ld_x64(taddr + (hi ? 0 : 64), y);
+          ptx::tmem_ld_wait(v, y);
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar_acc_empty(acc));
           {
-            uint32_t v[64];
-            ptx::tmem_ld_x64(taddr + (hi ? 64 : 0), v);
-            ptx::tmem_ld_wait(v);
             if (hi) {
 #pragma unroll
               for (int c = 0; c < 16; ++c)
@@ -680,9 +698,6 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
               }
             }
           }
-          uint32_t y[64];  // this warp's own position: hi position 0, lo position 1
-          ptx::tmem_ld_x64(taddr + (hi ? 0 : 64), y);
-          ptx::tmem_ld_wait(y);
           ptx::named_bar_sync(3, 128);  // both halves are parked
           const int pp = hi ? 0 : 1;
           const int row = pp * 64 + h;
@@ -825,8 +840,10 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive(bar_ob_full(b));
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar_acc_empty(acc));
+      if (!stk) {  // the stacked path releases its accumulator right after its TMEM loads
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_acc_empty(acc));
+      }
     }
     if (BWD && ok) {
       // This CTA's dM share: the sum of the diagonal nh x nh blocks of D2. The
