@@ -141,15 +141,13 @@ struct Tile {
   bool has_pe;
 };
 
+// Tile (rt, ct): row tile rt, channel tile ct.
 template <bool BWD>
-__device__ __forceinline__ Tile decode_tile(const PostmixParams& p, int64_t t) {
+__device__ __forceinline__ Tile make_tile(const PostmixParams& p, int rt, int ct) {
   using C = KCfg<BWD>;
   Tile x;
-  // 32-bit division: the host guarantees n_tiles < 2^31 (64-bit division here
-  // sits on the MMA issuer's critical path once per tile and is slow)
-  const uint32_t tu = static_cast<uint32_t>(t);
-  x.rt = static_cast<int>(tu / static_cast<uint32_t>(p.n_ct));
-  x.ct = static_cast<int>(tu - static_cast<uint32_t>(x.rt) * static_cast<uint32_t>(p.n_ct));
+  x.rt = rt;
+  x.ct = ct;
   x.row0 = x.rt * p.R;
   x.c0 = x.ct * C::NC;
   const int left = p.d - x.c0;
@@ -157,6 +155,16 @@ __device__ __forceinline__ Tile decode_tile(const PostmixParams& p, int64_t t) {
   x.s0 = static_cast<int64_t>(x.rt) * p.P;
   x.has_pe = (p.nope / C::NC) == x.ct;
   return x;
+}
+
+// Tile t of the row-major (row tile, channel tile) order.
+template <bool BWD>
+__device__ __forceinline__ Tile decode_tile(const PostmixParams& p, int64_t t) {
+  // 32-bit division: the host guarantees n_tiles < 2^31 (64-bit division here
+  // sits on the MMA issuer's critical path once per tile and is slow)
+  const uint32_t tu = static_cast<uint32_t>(t);
+  const uint32_t rt = tu / static_cast<uint32_t>(p.n_ct);
+  return make_tile<BWD>(p, static_cast<int>(rt), static_cast<int>(tu - rt * static_cast<uint32_t>(p.n_ct)));
 }
 
 __device__ __forceinline__ void record_fault(unsigned code, volatile int* abort_flag) {
@@ -218,21 +226,23 @@ __device__ __forceinline__ bool group_wait(uint32_t bar, uint32_t parity, volati
 // positions array is given (rows past sq, which are never stored, take pos0).
 // The angle is reduced exactly in 64-bit fixed point: F[i] = f_i / (2 pi) * 2^64,
 // pos * F[i] mod 2^64 is the fractional turn count (two's complement, so a
-// negative position works too); its top 32 bits give a turn in [-1/2, 1/2)
-// that sincospif evaluates.
+// negative position works too); its top 32 bits give an angle in [-pi, pi),
+// where the hardware sine / cosine (__sincosf) is accurate to 2^-21.4
+// absolute, far below the bf16 rounding of the outputs.
 __device__ __forceinline__ void fill_rot_table(float2* tab, const uint64_t* F, const PostmixParams& p,
                                                int64_t s0, int half, int tid, int nthr) {
   const int n = p.P * half;
+  const bool half32 = half == 32;  // the common pe = 64: no division
   for (int k = tid; k < n; k += nthr) {
-    const int pl = k / half;
+    const int pl = half32 ? (k >> 5) : k / half;
     const int i = k - pl * half;
     const int64_t s = s0 + pl;
     const int64_t rel = p.pos ? (s < p.sq ? static_cast<int64_t>(__ldg(p.pos + s)) : 0) : s;
     const uint64_t turns = static_cast<uint64_t>(p.pos0 + rel) * F[i];
     const int32_t ti = static_cast<int32_t>(turns >> 32);
-    const float tf = static_cast<float>(ti) * 2.3283064365386963e-10f;  // 2^-32
+    const float tf = static_cast<float>(ti) * 2.3283064365386963e-10f;  // turns, 2^-32 units
     float sn, cs;
-    sincospif(2.0f * tf, &sn, &cs);
+    __sincosf(6.28318530717958648f * tf, &sn, &cs);
     tab[k] = make_float2(cs, sn);
   }
 }
@@ -610,6 +620,13 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
     const float sgn = BWD ? 1.f : -1.f;  // rope (+a) for dO, inverse rope (-a) for Y
     uint32_t n = 0;  // output chunk counter (output ring position)
     bool ok = true;
+    // backward: the next tile's (row tile, channel tile), advanced without a division
+    int e_rt = 0, e_ct = 0;
+    if (BWD) {
+      const Tile x0 = decode_tile<BWD>(p, t_begin);
+      e_rt = x0.rt;
+      e_ct = x0.ct;
+    }
     for (uint32_t i = 0; ok; ++i) {
       if (BWD && t_begin + i >= t_end) break;
       const int acc = acc_of(i);
@@ -643,7 +660,11 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
         }
         break;
       }
-      const Tile x = decode_tile<BWD>(p, t);
+      const Tile x = BWD ? make_tile<BWD>(p, e_rt, e_ct) : decode_tile<BWD>(p, t);
+      if (BWD && ++e_ct == p.n_ct) {
+        e_ct = 0;
+        ++e_rt;
+      }
       const int pcol = p.nope - x.c0;  // tile-relative column of the first pe channel
       if (x.has_pe) {
         fill_rot_table(tab, F, p, x.s0, half, e, 128);
