@@ -1,10 +1,15 @@
 """Run the library's kernels on a seeded synthetic workload (for profiling).
 
     python -m partial_inverse_rope_gb300.run_workload --ops fwd,bwd --sq 4096 --nh 64 --reps 2
+    python -m partial_inverse_rope_gb300.run_workload --config sweep_nh128 --ops fwd,bwd --time
 
 Each repetition calls the listed operations once, in the order given, on the
 same resident inputs; the process exits non-zero if a kernel's watchdog fired.
 Used to capture ncu profiles of one kernel on a case small enough to replay.
+With --time, each call is timed with CUDA events on its stream (after 3
+untimed repetitions; a 512 MiB buffer is rewritten between timed calls so that
+inputs smaller than the L2 are not served from it) and the median per call is
+printed with the algorithmic GB/s.
 """
 
 from __future__ import annotations
@@ -28,11 +33,17 @@ def main(argv=None):
     ap.add_argument("--pos0", type=int, default=16384)
     ap.add_argument("--remap-rows", type=int, default=16384, help="rows of the remap table (b*sq)")
     ap.add_argument("--reps", type=int, default=2)
+    ap.add_argument("--config", choices=sorted(W.POSTMIX_CONFIGS), default=None,
+                    help="take sq/nh/nope/pe/pos0 from a named config")
+    ap.add_argument("--time", action="store_true", help="time each call (median over --reps)")
     args = ap.parse_args(argv)
 
     ops = [o.strip() for o in args.ops.split(",") if o.strip()]
     dev = torch.device("cuda", 0)
-    c = W.PostmixConfig("workload", sq=args.sq, nh=args.nh, nope=args.nope, pe=args.pe, pos0=args.pos0)
+    if args.config:
+        c = W.POSTMIX_CONFIGS[args.config]
+    else:
+        c = W.PostmixConfig("workload", sq=args.sq, nh=args.nh, nope=args.nope, pe=args.pe, pos0=args.pos0)
     O, dY, M = W.postmix_inputs(c, device=dev)
     Y, dO = torch.empty_like(O), torch.empty_like(O)
     dM = torch.empty(c.nh, c.nh, dtype=torch.float32, device=dev)
@@ -42,17 +53,39 @@ def main(argv=None):
                       topk=2048, seqlen_kv=16384)
     idx = W.kv_index_table(R, device=dev) if "remap" in ops else None
     out = torch.empty_like(idx) if idx is not None else None
-    for _ in range(args.reps):
+    def call(op):
+        if op == "fwd":
+            ir.invrope_postmix_fwd(O, M, c.pos0, c.nope, c.pe, c.theta, Y=Y)
+        elif op == "bwd":
+            ir.invrope_postmix_bwd(dY, O, M, c.pos0, c.nope, c.pe, c.theta, dO=dO, dM=dM, workspace=ws)
+        elif op == "remap":
+            ir.kv_idx_local_to_global(idx, R.sq, R.seqlen_kv, out=out)
+        else:
+            raise SystemExit(f"unknown op {op}")
+
+    if not args.time:
+        for _ in range(args.reps):
+            for op in ops:
+                call(op)
+        torch.cuda.synchronize()
+    else:
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        nbytes = {"fwd": c.fwd_bytes(), "bwd": c.bwd_bytes(), "remap": R.bytes()}
         for op in ops:
-            if op == "fwd":
-                ir.invrope_postmix_fwd(O, M, c.pos0, c.nope, c.pe, c.theta, Y=Y)
-            elif op == "bwd":
-                ir.invrope_postmix_bwd(dY, O, M, c.pos0, c.nope, c.pe, c.theta, dO=dO, dM=dM, workspace=ws)
-            elif op == "remap":
-                ir.kv_idx_local_to_global(idx, R.sq, R.seqlen_kv, out=out)
-            else:
-                raise SystemExit(f"unknown op {op}")
-    torch.cuda.synchronize()
+            for _ in range(3):
+                call(op)
+            times = []
+            for _ in range(max(1, args.reps)):
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                call(op)
+                e1.record()
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1) * 1e3)
+            us = sorted(times)[len(times) // 2]
+            print(f"{c.name} {op}: sq={c.sq} nh={c.nh} d={c.d} median {us:.2f} us over {len(times)} calls, "
+                  f"{nbytes[op] / (us * 1e-6) / 1e9:.1f} GB/s algorithmic")
     fault = ir.invrope_take_device_fault()
     print(f"ran {args.reps} x {ops} at sq={c.sq} nh={c.nh} d={c.d}; watchdog fault code {fault}")
     return 1 if fault else 0
