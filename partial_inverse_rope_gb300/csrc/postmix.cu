@@ -871,31 +871,54 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
       // input ring is free once every MMA has completed.
       if (group_wait(bar_d2, 0, abort_flag, (kRoleEpilogue << 8) | kBarD2, e == 0, slot_d2, 1)) {
         ptx::tc_fence_after();
-        // red[h * (R + 1) + r] = D2[r][pl*nh + h]: consecutive rows -> consecutive
-        // words; the odd row stride keeps the transposed reads below conflict-free
-        float* red = reinterpret_cast<float*>(gbase + C::kOffStage);
-        const int rs = p.R + 1;
-        const int lo = pl * p.nh;
-        for (int j0 = 0; j0 < 128; j0 += 32) {
-          uint32_t v[32];
-          ptx::tmem_ld_x32(tmem_base + lane_addr + C::kD2Col + j0, v);
-          ptx::tmem_ld_wait(v);
-          if (row_ok) {
+        if (p.P == 1) {
+          // one position per tile: row r's D2 row is its partial row, straight from TMEM
+          float* dst = p.ws + (static_cast<int64_t>(blockIdx.x) * p.R + r) * p.nh;
+          for (int j0 = 0; j0 < 128; j0 += 32) {
+            uint32_t v[32];
+            ptx::tmem_ld_x32(tmem_base + lane_addr + C::kD2Col + j0, v);
+            ptx::tmem_ld_wait(v);
+            if (row_ok && j0 < p.nh) {
+              if (j0 + 32 <= p.nh && ((p.nh & 3) == 0)) {
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-              const int j = j0 + jj;
-              if (j >= lo && j < lo + p.nh) red[(j - lo) * rs + r] = __uint_as_float(v[jj]);
+                for (int u = 0; u < 8; ++u)
+                  *reinterpret_cast<float4*>(dst + j0 + 4 * u) =
+                      make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                  __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+              } else {
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj)
+                  if (j0 + jj < p.nh) dst[j0 + jj] = __uint_as_float(v[jj]);
+              }
             }
           }
-        }
-        ptx::named_bar_sync(1, 128);
-        const int nn = p.nh * p.nh;
-        // consecutive threads take consecutive h: coalesced partial rows
-        for (int idx = e; idx < nn; idx += 128) {
-          const int g = idx / p.nh, h = idx - g * p.nh;
-          float s = 0.f;
-          for (int q = 0; q < p.P; ++q) s += red[h * rs + q * p.nh + g];
-          p.ws[static_cast<int64_t>(blockIdx.x) * nn + g * p.nh + h] = s;
+        } else {
+          // red[h * (R + 1) + r] = D2[r][pl*nh + h]: consecutive rows -> consecutive
+          // words; the odd row stride keeps the transposed reads below conflict-free
+          float* red = reinterpret_cast<float*>(gbase + C::kOffStage);
+          const int rs = p.R + 1;
+          const int lo = pl * p.nh;
+          for (int j0 = 0; j0 < 128; j0 += 32) {
+            uint32_t v[32];
+            ptx::tmem_ld_x32(tmem_base + lane_addr + C::kD2Col + j0, v);
+            ptx::tmem_ld_wait(v);
+            if (row_ok) {
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj) {
+                const int j = j0 + jj;
+                if (j >= lo && j < lo + p.nh) red[(j - lo) * rs + r] = __uint_as_float(v[jj]);
+              }
+            }
+          }
+          ptx::named_bar_sync(1, 128);
+          const int nn = p.nh * p.nh;
+          // consecutive threads take consecutive h: coalesced partial rows
+          for (int idx = e; idx < nn; idx += 128) {
+            const int g = idx / p.nh, h = idx - g * p.nh;
+            float s = 0.f;
+            for (int q = 0; q < p.P; ++q) s += red[h * rs + q * p.nh + g];
+            p.ws[static_cast<int64_t>(blockIdx.x) * nn + g * p.nh + h] = s;
+          }
         }
       }
     }
