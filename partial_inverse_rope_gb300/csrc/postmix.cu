@@ -75,16 +75,18 @@ enum : unsigned { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleTrans
 enum : unsigned { kBarFull = 1, kBarEmpty, kBarAccFull, kBarAccEmpty, kBarXFull, kBarXEmpty,
                   kBarD2, kBarDone, kBarXGo, kBarOut };
 
-template <bool BWD>
+// WIDE (backward with one position per tile, nh > 64): 128-channel tiles, so
+// each head-mix MMA has N = 128 and a tile needs half as many of them.
+template <bool BWD, bool WIDE = false>
 struct KCfg {
-  static constexpr int NC = BWD ? 64 : 128;              // channels per tile
+  static constexpr int NC = (BWD && !WIDE) ? 64 : 128;   // channels per tile
   static constexpr int kChunks = NC / kChunkCols;
   static constexpr int kTensorTile = kChunks * kChunkBytes;
   static constexpr int kStageBytes = (BWD ? 2 : 1) * kTensorTile;   // input ring entry
-  static constexpr int kStages = 4;                      // input ring
+  static constexpr int kStages = WIDE ? 2 : 4;           // input ring (bytes in flight alike)
   static constexpr int kOutBufs = BWD ? 3 : 5;           // output ring of 64-channel chunks
   static constexpr int kOutInflight = kOutBufs - 2;      // TMA stores left reading smem
-  static constexpr int kNumAcc = BWD ? 4 : 3;
+  static constexpr int kNumAcc = BWD ? (WIDE ? 2 : 4) : 3;
   // TMEM columns: accumulators, then dM (bwd), then A hi (64) and A lo (64)
   static constexpr int kD2Col = kNumAcc * NC;
   static constexpr int kACol = 384;
@@ -99,7 +101,7 @@ struct KCfg {
   static constexpr int kXloBytes = BWD ? kChunkBytes : 0;
   // bwd, stacked mix: fp32 exchange rows between the epilogue warp pairs (64 x 256 B)
   static constexpr int kOffXch = kOffXlo + kXloBytes;
-  static constexpr int kXchBytes = BWD ? 64 * 256 : 0;
+  static constexpr int kXchBytes = (BWD && !WIDE) ? 64 * 256 : 0;
   static constexpr int kTabBytes = kPosPerTileMax * kMaxHalf * 8;
   static constexpr int kOffTabEpi = kOffXch + kXchBytes;
   static constexpr int kOffTabXf = kOffTabEpi + kTabBytes;
@@ -142,9 +144,9 @@ struct Tile {
 };
 
 // Tile (rt, ct): row tile rt, channel tile ct.
-template <bool BWD>
+template <bool BWD, bool WIDE = false>
 __device__ __forceinline__ Tile make_tile(const PostmixParams& p, int rt, int ct) {
-  using C = KCfg<BWD>;
+  using C = KCfg<BWD, WIDE>;
   Tile x;
   x.rt = rt;
   x.ct = ct;
@@ -158,13 +160,13 @@ __device__ __forceinline__ Tile make_tile(const PostmixParams& p, int rt, int ct
 }
 
 // Tile t of the row-major (row tile, channel tile) order.
-template <bool BWD>
+template <bool BWD, bool WIDE = false>
 __device__ __forceinline__ Tile decode_tile(const PostmixParams& p, int64_t t) {
   // 32-bit division: the host guarantees n_tiles < 2^31 (64-bit division here
   // sits on the MMA issuer's critical path once per tile and is slow)
   const uint32_t tu = static_cast<uint32_t>(t);
   const uint32_t rt = tu / static_cast<uint32_t>(p.n_ct);
-  return make_tile<BWD>(p, static_cast<int>(rt), static_cast<int>(tu - rt * static_cast<uint32_t>(p.n_ct)));
+  return make_tile<BWD, WIDE>(p, static_cast<int>(rt), static_cast<int>(tu - rt * static_cast<uint32_t>(p.n_ct)));
 }
 
 __device__ __forceinline__ void record_fault(unsigned code, volatile int* abort_flag) {
@@ -294,10 +296,10 @@ struct ARow {
   }
 };
 
-template <bool BWD>
-__global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
+template <bool BWD, bool WIDE = false>
+__global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
     postmix_kernel(const __grid_constant__ PostmixParams p) {
-  using C = KCfg<BWD>;
+  using C = KCfg<BWD, WIDE>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -341,8 +343,8 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
   // Accumulator ring: NA accumulators of NC columns, or 2 of 128 columns for the
   // stacked backward mix (the same 256 TMEM columns).
   const bool stk = BWD && p.stacked != 0;
-  static_assert(!BWD || NA == 4, "the backward ring is indexed with shifts");
-  const uint32_t na_sh = stk ? 1u : 2u;
+  static_assert(!BWD || NA == 4 || NA == 2, "the backward ring is indexed with shifts");
+  const uint32_t na_sh = (stk || NA == 2) ? 1u : 2u;
   const uint32_t acc_cols = stk ? 128u : static_cast<uint32_t>(C::NC);
   auto acc_of = [&](uint32_t i) { return static_cast<int>(BWD ? i & ((1u << na_sh) - 1u) : i % NA); };
   auto acc_phase = [&](uint32_t i) { return BWD ? (i >> na_sh) & 1u : (i / NA) & 1u; };
@@ -485,7 +487,7 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
           t_next = static_cast<int64_t>(atomicAdd(p.sched, 1u));
           stage_tile[st] = static_cast<int>(t);
         }
-        const Tile x = decode_tile<BWD>(p, t);
+        const Tile x = decode_tile<BWD, WIDE>(p, t);
         const uint32_t bytes = static_cast<uint32_t>(x.nch * p.R * 128 * (BWD ? 2 : 1));
         ptx::mbar_arrive_expect_tx(bar_full(st), bytes);
         const uint32_t sa = stage_addr(st);
@@ -556,7 +558,7 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
           ptx::tc_commit(bar_acc_full(acc));
           break;
         }
-        const Tile x = decode_tile<BWD>(p, t);
+        const Tile x = decode_tile<BWD, WIDE>(p, t);
         // The transform warps only see pe tiles; this thread has observed every
         // stage phase in order, so it tells them when the pe tile has landed.
         if (BWD && x.has_pe) ptx::mbar_arrive(bar_x_go);
@@ -623,7 +625,7 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
     // backward: the next tile's (row tile, channel tile), advanced without a division
     int e_rt = 0, e_ct = 0;
     if (BWD) {
-      const Tile x0 = decode_tile<BWD>(p, t_begin);
+      const Tile x0 = decode_tile<BWD, WIDE>(p, t_begin);
       e_rt = x0.rt;
       e_ct = x0.ct;
     }
@@ -660,7 +662,7 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
         }
         break;
       }
-      const Tile x = BWD ? make_tile<BWD>(p, e_rt, e_ct) : decode_tile<BWD>(p, t);
+      const Tile x = BWD ? make_tile<BWD, WIDE>(p, e_rt, e_ct) : decode_tile<BWD, WIDE>(p, t);
       if (BWD && ++e_ct == p.n_ct) {
         e_ct = 0;
         ++e_rt;
@@ -931,7 +933,7 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
       for (uint32_t i = 0; ok; ++i) {
         if (BWD && t_begin + i >= t_end) break;
         const int64_t tb = t_begin + i;
-        const int nk = BWD ? decode_tile<BWD>(p, tb).nch : 1;  // forward: one chunk per hand-off
+        const int nk = BWD ? decode_tile<BWD, WIDE>(p, tb).nch : 1;  // forward: one chunk per hand-off
         for (int kk = 0; kk < nk; ++kk, ++n) {
           const int b = static_cast<int>(n % OB);
           if (!wait_bar(bar_ob_full(b), (n / OB) & 1u, abort_flag,
@@ -945,7 +947,7 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
             break;
           }
           const int k = BWD ? kk : ob_chunk[b];
-          const Tile x = decode_tile<BWD>(p, t);
+          const Tile x = decode_tile<BWD, WIDE>(p, t);
           ptx::tma_store_2d(&p.tm_out, out_addr(b), x.c0 + k * kChunkCols, x.row0);
           ptx::bulk_commit();
           // keep kIn stores reading; recycle the buffer of the oldest finished one
@@ -966,7 +968,7 @@ __global__ void __launch_bounds__(KCfg<BWD>::kThreads, 1)
       int npe = 0;
       uint32_t i = 0;
       for (int64_t t = t_begin; t < t_end; ++t, ++i) {
-        const Tile x = decode_tile<BWD>(p, t);
+        const Tile x = decode_tile<BWD, WIDE>(p, t);
         if (!x.has_pe) continue;
         const int st = static_cast<int>(i % S);
         const uint32_t ph = (i / S) & 1u;
@@ -1145,15 +1147,16 @@ int check_shape(int64_t sq, int nh, int nope, int pe, int nc, Shape* s) {
   return INVROPE_OK;
 }
 
-template <bool BWD>
+template <bool BWD, bool WIDE = false>
 int ensure_smem_attr(int device) {
   static std::mutex mu;
   static bool done[64] = {};
   std::lock_guard<std::mutex> lock(mu);
   if (device < 0 || device >= 64) return INVROPE_ERR_DEVICE;
   if (!done[device]) {
-    const cudaError_t err = cudaFuncSetAttribute(postmix_kernel<BWD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 KCfg<BWD>::kSmemAlloc);
+    const cudaError_t err = cudaFuncSetAttribute(postmix_kernel<BWD, WIDE>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 KCfg<BWD, WIDE>::kSmemAlloc);
     if (err != cudaSuccess) return cuda_fail(err);
     done[device] = true;
   }
@@ -1184,6 +1187,10 @@ int sched_slot(int device, unsigned int** out) {
 
 // Grid size of the backward kernel (one dM partial per CTA).
 static int64_t bwd_grid(const Shape& s, int sms) { return s.n_tiles < sms ? s.n_tiles : sms; }
+
+// The backward runs 128-channel tiles when a tile holds one position (nh > 64).
+static bool bwd_wide(int nh) { return nh > 64; }
+static int bwd_nc(int nh) { return bwd_wide(nh) ? KCfg<true, true>::NC : KCfg<true>::NC; }
 
 }  // namespace invrope
 
@@ -1251,7 +1258,7 @@ extern "C" int invrope_postmix_fwd(const void* O, const float* M, void* Y, int64
 
 extern "C" size_t invrope_postmix_bwd_workspace_bytes(int64_t sq, int nh, int nope, int pe) {
   Shape s;
-  if (check_shape(sq, nh, nope, pe, KCfg<true>::NC, &s) != INVROPE_OK) return 0;
+  if (check_shape(sq, nh, nope, pe, bwd_nc(nh), &s) != INVROPE_OK) return 0;
   DeviceInfo dev;
   if (current_device(&dev) != INVROPE_OK) return 0;
   const int64_t grid = sq == 0 ? 1 : bwd_grid(s, dev.sms);
@@ -1263,7 +1270,7 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
                                       int nope, int pe, const int32_t* positions, int64_t pos0, double theta,
                                       struct CUstream_st* stream) {
   Shape s;
-  int st = check_shape(sq, nh, nope, pe, KCfg<true>::NC, &s);
+  int st = check_shape(sq, nh, nope, pe, bwd_nc(nh), &s);
   if (st != INVROPE_OK) return st;
   if ((st = check_mix_args(nh, gs, positions, pos0, theta)) != INVROPE_OK) return st;
   if (!M || !dM || !aligned(M, 4) || !aligned(dM, 4)) return INVROPE_ERR_INVALID_ARG;
@@ -1289,7 +1296,9 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
   }
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (grid > 0) {
-    if ((st = ensure_smem_attr<true>(dev.device)) != INVROPE_OK) return st;
+    const bool wide = bwd_wide(nh);
+    if ((st = wide ? ensure_smem_attr<true, true>(dev.device) : ensure_smem_attr<true>(dev.device)) != INVROPE_OK)
+      return st;
     PostmixParams p;
     std::memset(&p, 0, sizeof(p));
     const int d = nope + pe;
@@ -1310,11 +1319,15 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
     p.R = s.R;
     p.n_ct = s.n_ct;
     // stacked head mix: two positions of 64 heads per tile, pe block = one chunk
-    p.stacked = (nh == 64 && pe == kChunkCols && nope % kChunkCols == 0) ? 1 : 0;
+    p.stacked = (!wide && nh == 64 && pe == kChunkCols && nope % kChunkCols == 0) ? 1 : 0;
     p.pos = positions;
     p.gs = gs;
     fill_freq(p.F, pe, theta);
-    postmix_kernel<true><<<static_cast<unsigned>(grid), KCfg<true>::kThreads, KCfg<true>::kSmemAlloc, cs>>>(p);
+    if (wide)
+      postmix_kernel<true, true>
+          <<<static_cast<unsigned>(grid), KCfg<true, true>::kThreads, KCfg<true, true>::kSmemAlloc, cs>>>(p);
+    else
+      postmix_kernel<true><<<static_cast<unsigned>(grid), KCfg<true>::kThreads, KCfg<true>::kSmemAlloc, cs>>>(p);
     if ((st = check_launch()) != INVROPE_OK) return st;
   }
   // Programmatic dependent launch: the reduction grid's launch is processed

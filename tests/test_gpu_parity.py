@@ -64,6 +64,9 @@ SHAPES = [
     (301, 64, 480, 32, 9, 1e4),       # nh = 64 with pe < 64: block-diagonal backward mix
     (130, 64, 448, 64, 2**31 + 12345, 1e4),  # positions beyond 2^31 (exact angle reduction)
     (33, 128, 448, 64, 0, 5e5),       # 128 heads, another rotary base
+    (70, 100, 448, 64, 3, 1e4),       # nh = 100: 128-channel backward tiles of R = 100 rows
+    (40, 128, 64, 64, 0, 1e4),        # d = 128: one 128-channel tile per row tile, every tile has pe
+    (50, 96, 480, 32, 5, 1e4),        # 128-channel backward tiles, pe = 32 in the last 64-channel chunk
     (2053, 16, 448, 64, 0, 1e4),      # mid-like, ragged
 ]
 
