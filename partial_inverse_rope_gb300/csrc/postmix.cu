@@ -115,6 +115,7 @@ struct KCfg {
   static_assert(kNumAcc * NC + (BWD ? 128 : 0) <= kACol, "TMEM budget");
   static_assert(kStages * kStageBytes >= 128 * 129 * 4, "dM partial reduction reuses the input ring");
   static_assert(kOutInflight >= 1, "at least one store in flight");
+  static_assert(kOffFreq - kOffOut >= 128 * 129 * 4, "M is staged in the output ring and the buffers after it");
 };
 
 struct PostmixParams {
@@ -380,76 +381,9 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
     ptx::tmem_alloc(base + C::kOffMisc, C::kTmemCols);
     ptx::tmem_relinquish();
   }
-  if (BWD)
-    for (uint32_t o = threadIdx.x * 16u; o < static_cast<uint32_t>(kChunkBytes); o += blockDim.x * 16u)
-      ptx::st_shared_v4(base + C::kOffXlo + o, 0u, 0u, 0u, 0u);
   if (threadIdx.x < half) F[threadIdx.x] = p.F[threadIdx.x];
-  // M staged in the (still idle) input ring for the A build below, row stride
-  // nh + 1; four independent loads in flight per thread. A grouped mix
-  // (p.M = [nh/gs, gs, gs]) is expanded to its block-diagonal [nh, nh] form.
-  float* Ms = reinterpret_cast<float*>(gbase + C::kOffStage);
-  {
-    const int nn = p.nh * p.nh;
-    for (int k0 = threadIdx.x; k0 < nn; k0 += 4 * blockDim.x) {
-      float v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int k = k0 + u * blockDim.x;
-        const int g = k / p.nh, h = k - (k / p.nh) * p.nh;
-        const int b0 = (g / p.gs) * p.gs;  // first head of g's group
-        const bool in = k < nn && h >= b0 && h < b0 + p.gs;
-        v[u] = in ? __ldg(p.M + static_cast<int64_t>(b0) * p.gs + (g - b0) * p.gs + (h - b0)) : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int k = k0 + u * blockDim.x;
-        if (k < nn) Ms[(k / p.nh) * (p.nh + 1) + k % p.nh] = v[u];
-      }
-    }
-  }
-  ptx::fence_proxy_async_smem();
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-
-  if (warp >= 2 && warp < 6) {
-    // A in TMEM: lane m holds row m; column kACol + hl*64 + j/2 holds the bf16
-    // pair (j, j+1) of the hi (hl = 0) or lo (hl = 1) term, lower j in the low half.
-    const uint32_t quad = static_cast<uint32_t>(warp & 3);
-    const int m = static_cast<int>(quad * 32) + lane;
-    const uint32_t row_addr = tmem_base + ((quad * 32u) << 16) + C::kACol;
-    if (BWD && p.stacked) {
-      // stacked A: lane m < 64 holds M^T_hi row m, lane 64 + h holds M^T_lo row h
-      const int h = m & 63;
-      uint32_t w[32];
-#pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const float v0 = Ms[(2 * q) * 65 + h], v1 = Ms[(2 * q + 1) * 65 + h];
-        const uint32_t hw = ptx::pack_bf16x2(v0, v1);
-        w[q] = m < 64 ? hw : ptx::pack_bf16x2(v0 - ptx::bf16_lo_f32(hw), v1 - ptx::bf16_hi_f32(hw));
-      }
-      ptx::tmem_st_x32(row_addr, w);
-    } else {
-      const ARow<BWD> arow(p, Ms, m);
-      for (int hl = 0; hl < 2; ++hl)
-        for (int kh = 0; kh < 2; ++kh) {
-          uint32_t w[32];
-#pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const int j = kh * 64 + 2 * q;
-            const float v0 = arow.at(j), v1 = arow.at(j + 1);
-            const uint32_t h = ptx::pack_bf16x2(v0, v1);
-            w[q] = hl == 0 ? h : ptx::pack_bf16x2(v0 - ptx::bf16_lo_f32(h), v1 - ptx::bf16_hi_f32(h));
-          }
-          ptx::tmem_st_x32(row_addr + hl * 64 + kh * 32, w);
-        }
-    }
-    ptx::tmem_st_wait();
-  }
-  __syncthreads();  // the staged M is dead from here on
   // Rows >= R of every 64-channel box are never loaded and must read as 0
-  // (the MMA's K range covers them); X_lo starts at 0 on its nope channels.
+  // (the MMA's K range covers them).
   if (p.R < kRowsMax) {
     const uint32_t tail = static_cast<uint32_t>(kRowsMax - p.R) * 128u;  // bytes per box
     const uint32_t nbox = static_cast<uint32_t>(S * C::kStageBytes / kChunkBytes);
@@ -460,16 +394,96 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
 
   const int64_t G = gridDim.x;
   const int64_t t_begin = p.n_tiles * blockIdx.x / G;
   const int64_t t_end = p.n_tiles * (blockIdx.x + 1) / G;
 
+  // The producer starts streaming right away; meanwhile every other warp
+  // stages M, builds A in TMEM and (backward) clears X_lo, synchronised by
+  // named barrier 4 (all warps but the producer).
+  if (warp != 0) {
+    const int nthr = static_cast<int>(blockDim.x) - 32, tid = static_cast<int>(threadIdx.x) - 32;
+    // M staged with row stride nh + 1 in the output ring and the buffers after
+    // it (idle until the first tile is mixed); all of a thread's loads are in
+    // flight together. A grouped mix (p.M = [nh/gs, gs, gs]) is expanded to
+    // its block-diagonal [nh, nh] form.
+    float* Ms = reinterpret_cast<float*>(gbase + C::kOffOut);
+    {
+      constexpr int kBatch = 16;
+      const int nn = p.nh * p.nh;
+      for (int k0 = tid; k0 < nn; k0 += kBatch * nthr) {
+        float v[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int k = k0 + u * nthr;
+          const int g = k / p.nh, h = k - g * p.nh;
+          const int b0 = (g / p.gs) * p.gs;  // first head of g's group
+          const bool in = k < nn && h >= b0 && h < b0 + p.gs;
+          v[u] = in ? __ldg(p.M + static_cast<int64_t>(b0) * p.gs + (g - b0) * p.gs + (h - b0)) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int k = k0 + u * nthr;
+          const int g = k / p.nh;
+          if (k < nn) Ms[g * (p.nh + 1) + (k - g * p.nh)] = v[u];
+        }
+      }
+    }
+    ptx::named_bar_sync(4, nthr);
+    if (warp >= 2 && warp < 6) {
+      // A in TMEM: lane m holds row m; column kACol + hl*64 + j/2 holds the bf16
+      // pair (j, j+1) of the hi (hl = 0) or lo (hl = 1) term, lower j in the low half.
+      const uint32_t quad = static_cast<uint32_t>(warp & 3);
+      const int m = static_cast<int>(quad * 32) + lane;
+      const uint32_t row_addr = tmem_base + ((quad * 32u) << 16) + C::kACol;
+      if (BWD && p.stacked) {
+        // stacked A: lane m < 64 holds M^T_hi row m, lane 64 + h holds M^T_lo row h
+        const int h = m & 63;
+        uint32_t w[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          const float v0 = Ms[(2 * q) * 65 + h], v1 = Ms[(2 * q + 1) * 65 + h];
+          const uint32_t hw = ptx::pack_bf16x2(v0, v1);
+          w[q] = m < 64 ? hw : ptx::pack_bf16x2(v0 - ptx::bf16_lo_f32(hw), v1 - ptx::bf16_hi_f32(hw));
+        }
+        ptx::tmem_st_x32(row_addr, w);
+      } else {
+        const ARow<BWD> arow(p, Ms, m);
+        for (int hl = 0; hl < 2; ++hl)
+          for (int kh = 0; kh < 2; ++kh) {
+            uint32_t w[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+              const int j = kh * 64 + 2 * q;
+              const float v0 = arow.at(j), v1 = arow.at(j + 1);
+              const uint32_t h = ptx::pack_bf16x2(v0, v1);
+              w[q] = hl == 0 ? h : ptx::pack_bf16x2(v0 - ptx::bf16_lo_f32(h), v1 - ptx::bf16_hi_f32(h));
+            }
+            ptx::tmem_st_x32(row_addr + hl * 64 + kh * 32, w);
+          }
+      }
+      ptx::tmem_st_wait();
+    }
+    ptx::named_bar_sync(4, nthr);  // the staged M is dead from here on
+    // X_lo starts at 0 on its nope channels (it may overlap the staged M)
+    if (BWD)
+      for (uint32_t o = static_cast<uint32_t>(tid) * 16u; o < static_cast<uint32_t>(kChunkBytes);
+           o += static_cast<uint32_t>(nthr) * 16u)
+        ptx::st_shared_v4(base + C::kOffXlo + o, 0u, 0u, 0u, 0u);
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    ptx::named_bar_sync(4, nthr);
+    ptx::tc_fence_after();
+  }
+
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
-      // forward: tiles are claimed from the launch's counter, one claim ahead
-      int64_t t_next = BWD ? t_begin : static_cast<int64_t>(atomicAdd(p.sched, 1u));
+      // forward: the first tile is the block index, later ones are claimed
+      // from the launch's counter, one claim ahead
+      int64_t t_next = BWD ? t_begin : static_cast<int64_t>(blockIdx.x);
       for (uint32_t i = 0;; ++i) {
         const int st = static_cast<int>(i % S);
         const uint32_t ph = (i / S) & 1u;
@@ -484,7 +498,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
             ptx::mbar_arrive(bar_full(st));
             break;
           }
-          t_next = static_cast<int64_t>(atomicAdd(p.sched, 1u));
+          t_next = static_cast<int64_t>(gridDim.x) + static_cast<int64_t>(atomicAdd(p.sched, 1u));
           stage_tile[st] = static_cast<int>(t);
         }
         const Tile x = decode_tile<BWD, WIDE>(p, t);
