@@ -115,7 +115,6 @@ struct KCfg {
   static_assert(kNumAcc * NC + (BWD ? 128 : 0) <= kACol, "TMEM budget");
   static_assert(kStages * kStageBytes >= 128 * 129 * 4, "dM partial reduction reuses the input ring");
   static_assert(kOutInflight >= 1, "at least one store in flight");
-  static_assert(kOffFreq - kOffOut >= 128 * 129 * 4, "M is staged in the output ring and the buffers after it");
 };
 
 struct PostmixParams {
@@ -276,24 +275,22 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
-// Row m of A = blockdiag_P(M) (forward) or blockdiag_P(M^T) (backward): its
-// only nonzero columns are j in [b0, b0 + nh), b0 = (m / nh) * nh, for m < R.
-template <bool BWD>
-struct ARow {
-  const float* M;  // M staged in shared memory
-  int nh, b0, gi;
-  bool live;
-  __device__ __forceinline__ ARow(const PostmixParams& p, const float* Ms, int m) : M(Ms), nh(p.nh) {
-    live = m < p.R;
-    const int blk = live ? m / p.nh : 0;
-    b0 = blk * p.nh;
-    gi = m - b0;
+// One row or one column of the [nh, nh] head mix in its block-diagonal form
+// (a grouped mix, p.M = [nh/gs, gs, gs], is zero between groups), read from
+// p.M directly: it is a few KB and stays in L2 after the first thread block.
+struct MixLine {
+  const float* M;
+  int gs, b, f;  // group size; first head of the fixed index's group; fixed index - b
+  bool row;      // true: M[fixed][x]; false: M[x][fixed]
+  __device__ __forceinline__ MixLine(const PostmixParams& p, int fixed, bool is_row)
+      : M(p.M), gs(p.gs), row(is_row) {
+    b = (fixed / p.gs) * p.gs;
+    f = fixed - b;
   }
-  __device__ __forceinline__ float at(int j) const {
-    const unsigned gj = static_cast<unsigned>(j - b0);
-    if (!live || gj >= static_cast<unsigned>(nh)) return 0.f;
-    // staged with row stride nh + 1: lanes (consecutive gi) hit distinct banks
-    return BWD ? M[gj * (nh + 1) + gi] : M[gi * (nh + 1) + gj];
+  __device__ __forceinline__ float at(int x) const {  // 0 <= x < nh
+    const unsigned o = static_cast<unsigned>(x - b);
+    if (o >= static_cast<unsigned>(gs)) return 0.f;
+    return __ldg(M + static_cast<int64_t>(b) * gs + (row ? f * gs + static_cast<int>(o) : static_cast<int>(o) * gs + f));
   }
 };
 
@@ -401,73 +398,57 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
   const int64_t t_end = p.n_tiles * (blockIdx.x + 1) / G;
 
   // The producer starts streaming right away; meanwhile every other warp
-  // stages M, builds A in TMEM and (backward) clears X_lo, synchronised by
-  // named barrier 4 (all warps but the producer).
+  // builds A in TMEM and (backward) clears X_lo, then they meet at named
+  // barrier 4 (all warps but the producer).
   if (warp != 0) {
     const int nthr = static_cast<int>(blockDim.x) - 32, tid = static_cast<int>(threadIdx.x) - 32;
-    // M staged with row stride nh + 1 in the output ring and the buffers after
-    // it (idle until the first tile is mixed); all of a thread's loads are in
-    // flight together. A grouped mix (p.M = [nh/gs, gs, gs]) is expanded to
-    // its block-diagonal [nh, nh] form.
-    float* Ms = reinterpret_cast<float*>(gbase + C::kOffOut);
-    {
-      constexpr int kBatch = 16;
-      const int nn = p.nh * p.nh;
-      for (int k0 = tid; k0 < nn; k0 += kBatch * nthr) {
-        float v[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int k = k0 + u * nthr;
-          const int g = k / p.nh, h = k - g * p.nh;
-          const int b0 = (g / p.gs) * p.gs;  // first head of g's group
-          const bool in = k < nn && h >= b0 && h < b0 + p.gs;
-          v[u] = in ? __ldg(p.M + static_cast<int64_t>(b0) * p.gs + (g - b0) * p.gs + (h - b0)) : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int k = k0 + u * nthr;
-          const int g = k / p.nh;
-          if (k < nn) Ms[g * (p.nh + 1) + (k - g * p.nh)] = v[u];
-        }
-      }
-    }
-    ptx::named_bar_sync(4, nthr);
     if (warp >= 2 && warp < 6) {
       // A in TMEM: lane m holds row m; column kACol + hl*64 + j/2 holds the bf16
-      // pair (j, j+1) of the hi (hl = 0) or lo (hl = 1) term, lower j in the low half.
+      // pair (j, j+1) of the hi (hl = 0) or lo (hl = 1) term, lower j in the
+      // low half. Each thread reads its row's entries of M straight from L2,
+      // all loads of a 64-column half in flight together.
       const uint32_t quad = static_cast<uint32_t>(warp & 3);
       const int m = static_cast<int>(quad * 32) + lane;
       const uint32_t row_addr = tmem_base + ((quad * 32u) << 16) + C::kACol;
       if (BWD && p.stacked) {
         // stacked A: lane m < 64 holds M^T_hi row m, lane 64 + h holds M^T_lo row h
-        const int h = m & 63;
+        const MixLine col(p, m & 63, false);
+        float v[64];
+#pragma unroll
+        for (int q = 0; q < 64; ++q) v[q] = col.at(q);
         uint32_t w[32];
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
-          const float v0 = Ms[(2 * q) * 65 + h], v1 = Ms[(2 * q + 1) * 65 + h];
-          const uint32_t hw = ptx::pack_bf16x2(v0, v1);
-          w[q] = m < 64 ? hw : ptx::pack_bf16x2(v0 - ptx::bf16_lo_f32(hw), v1 - ptx::bf16_hi_f32(hw));
+          const uint32_t hw = ptx::pack_bf16x2(v[2 * q], v[2 * q + 1]);
+          w[q] = m < 64 ? hw : ptx::pack_bf16x2(v[2 * q] - ptx::bf16_lo_f32(hw), v[2 * q + 1] - ptx::bf16_hi_f32(hw));
         }
         ptx::tmem_st_x32(row_addr, w);
       } else {
-        const ARow<BWD> arow(p, Ms, m);
-        for (int hl = 0; hl < 2; ++hl)
-          for (int kh = 0; kh < 2; ++kh) {
-            uint32_t w[32];
+        // A = blockdiag_P(M) (forward) or blockdiag_P(M^T) (backward): row m
+        // (position m / nh, head m % nh) is nonzero on columns [pb, pb + nh) only
+        const bool live = m < p.R;
+        const int pb = live ? (m / p.nh) * p.nh : 0;
+        const MixLine line(p, m - pb, !BWD);  // forward: row of M; backward: column
+        for (int kh = 0; kh < 2; ++kh) {
+          float v[64];
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
-              const int j = kh * 64 + 2 * q;
-              const float v0 = arow.at(j), v1 = arow.at(j + 1);
-              const uint32_t h = ptx::pack_bf16x2(v0, v1);
-              w[q] = hl == 0 ? h : ptx::pack_bf16x2(v0 - ptx::bf16_lo_f32(h), v1 - ptx::bf16_hi_f32(h));
-            }
-            ptx::tmem_st_x32(row_addr + hl * 64 + kh * 32, w);
+          for (int q = 0; q < 64; ++q) {
+            const unsigned o = static_cast<unsigned>(kh * 64 + q - pb);
+            v[q] = (live && o < static_cast<unsigned>(p.nh)) ? line.at(static_cast<int>(o)) : 0.f;
           }
+          uint32_t whi[32], wlo[32];
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            whi[q] = ptx::pack_bf16x2(v[2 * q], v[2 * q + 1]);
+            wlo[q] = ptx::pack_bf16x2(v[2 * q] - ptx::bf16_lo_f32(whi[q]), v[2 * q + 1] - ptx::bf16_hi_f32(whi[q]));
+          }
+          ptx::tmem_st_x32(row_addr + kh * 32, whi);
+          ptx::tmem_st_x32(row_addr + 64 + kh * 32, wlo);
+        }
       }
       ptx::tmem_st_wait();
     }
-    ptx::named_bar_sync(4, nthr);  // the staged M is dead from here on
-    // X_lo starts at 0 on its nope channels (it may overlap the staged M)
+    // X_lo starts at 0 on its nope channels
     if (BWD)
       for (uint32_t o = static_cast<uint32_t>(tid) * 16u; o < static_cast<uint32_t>(kChunkBytes);
            o += static_cast<uint32_t>(nthr) * 16u)
