@@ -377,6 +377,12 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
   if (warp == 1) {
     ptx::tmem_alloc(base + C::kOffMisc, C::kTmemCols);
     ptx::tmem_relinquish();
+    // M into L2 ahead of the A build (128-byte lines); the warp reconverges
+    // before anything warp-collective follows
+    const char* mb = reinterpret_cast<const char*>(p.M);
+    const int mbytes = p.nh * p.gs * 4;
+    for (int o = lane * 128; o < mbytes; o += 32 * 128) ptx::prefetch_l2(mb + o);
+    __syncwarp();
   }
   if (threadIdx.x < half) F[threadIdx.x] = p.F[threadIdx.x];
   // Rows >= R of every 64-channel box are never loaded and must read as 0
@@ -429,7 +435,14 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
         const bool live = m < p.R;
         const int pb = live ? (m / p.nh) * p.nh : 0;
         const MixLine line(p, m - pb, !BWD);  // forward: row of M; backward: column
-        for (int kh = 0; kh < 2; ++kh) {
+        // the 64-column half holding the block of the warp's first row goes
+        // first, so that (nh = 64) every thread's loads go out in the first
+        // round; the order must be the same across the warp (tcgen05.st is
+        // warp-collective with one column address)
+        const int m0 = static_cast<int>(quad * 32);
+        const int kfirst = (m0 < p.R ? ((m0 / p.nh) * p.nh) >> 6 : 0) & 1;
+        for (int i = 0; i < 2; ++i) {
+          const int kh = i ^ kfirst;
           float v[64];
 #pragma unroll
           for (int q = 0; q < 64; ++q) {

@@ -20,6 +20,11 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 // griddep_wait() blocks until that grid has completed and its writes are visible.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Hint: bring the 128-byte line holding `ptr` (global memory) into L2.
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
