@@ -73,7 +73,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;         // bounded waits: 2 s
 // fault codes: role in bits 8-11, barrier kind in bits 0-7
 enum : unsigned { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleTransform = 4, kRoleStore = 5 };
 enum : unsigned { kBarFull = 1, kBarEmpty, kBarAccFull, kBarAccEmpty, kBarXFull, kBarXEmpty,
-                  kBarD2, kBarDone, kBarXGo, kBarOut };
+                  kBarD2, kBarDone, kBarXGo, kBarOut, kBarM };
 
 // WIDE (backward with one position per tile, nh > 64): 128-channel tiles, so
 // each head-mix MMA has N = 128 and a tile needs half as many of them.
@@ -107,7 +107,7 @@ struct KCfg {
   static constexpr int kOffTabXf = kOffTabEpi + kTabBytes;
   static constexpr int kOffFreq = kOffTabXf + (BWD ? kTabBytes : 0);
   static constexpr int kOffBars = kOffFreq + kMaxHalf * 8;
-  static constexpr int kNumBars = 2 * kStages + 2 * kOutBufs + 2 * kNumAcc + 5;
+  static constexpr int kNumBars = 2 * kStages + 2 * kOutBufs + 2 * kNumAcc + 6;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 192;      // tmem base, abort flag, wait slots, tile ids
   static constexpr int kSmemAlloc = kSmemBytes + 1024;   // slack to align the base
@@ -115,6 +115,7 @@ struct KCfg {
   static_assert(kNumAcc * NC + (BWD ? 128 : 0) <= kACol, "TMEM budget");
   static_assert(kStages * kStageBytes >= 128 * 129 * 4, "dM partial reduction reuses the input ring");
   static_assert(kOutInflight >= 1, "at least one store in flight");
+  static_assert(kOffFreq - kOffOut >= 128 * 128 * 4, "M is copied into the output ring and the buffers after it");
 };
 
 struct PostmixParams {
@@ -135,6 +136,7 @@ struct PostmixParams {
   int stacked;         // bwd, nh = 64, pe block = one whole chunk: stacked head mix (below)
   const int32_t* pos;  // per-row positions (pos0 is added), or null: row s sits at pos0 + s
   int gs;              // heads per group of the head mix (nh: one [nh, nh] matrix)
+  int m_bulk;          // forward: M is copied into shared memory by one bulk copy at start
 };
 
 struct Tile {
@@ -320,6 +322,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
   const uint32_t bar_d2 = bar_x_full + 16;
   const uint32_t bar_done = bar_x_full + 24;
   const uint32_t bar_x_go = bar_x_full + 32;
+  const uint32_t bar_m = bar_x_full + 40;  // M's bulk copy into shared memory
   auto stage_addr = [&](int s) { return base + C::kOffStage + static_cast<uint32_t>(s) * C::kStageBytes; };
   auto out_addr = [&](int b) { return base + C::kOffOut + static_cast<uint32_t>(b) * kChunkBytes; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
@@ -366,8 +369,15 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
     ptx::mbar_init(bar_d2, 1);
     ptx::mbar_init(bar_done, 1);
     ptx::mbar_init(bar_x_go, 1);
+    ptx::mbar_init(bar_m, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
+    // forward: M goes out first, ahead of every tile load; the A build waits on it
+    if (!BWD && p.m_bulk) {
+      const uint32_t mbytes = static_cast<uint32_t>(p.nh * p.gs * 4);
+      ptx::mbar_arrive_expect_tx(bar_m, mbytes);
+      ptx::bulk_load(base + C::kOffOut, p.M, mbytes, bar_m);
+    }
   }
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&p.tm_in0);
@@ -381,7 +391,8 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
     // before anything warp-collective follows
     const char* mb = reinterpret_cast<const char*>(p.M);
     const int mbytes = p.nh * p.gs * 4;
-    for (int o = lane * 128; o < mbytes; o += 32 * 128) ptx::prefetch_l2(mb + o);
+    if (BWD || !p.m_bulk)
+      for (int o = lane * 128; o < mbytes; o += 32 * 128) ptx::prefetch_l2(mb + o);
     __syncwarp();
   }
   if (threadIdx.x < half) F[threadIdx.x] = p.F[threadIdx.x];
@@ -416,6 +427,14 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
       const uint32_t quad = static_cast<uint32_t>(warp & 3);
       const int m = static_cast<int>(quad * 32) + lane;
       const uint32_t row_addr = tmem_base + ((quad * 32u) << 16) + C::kACol;
+      // forward, nh a multiple of 64, ungrouped: M in shared memory once its
+      // bulk copy has landed (the copy left ahead of every tile load), read as
+      // 16-byte row vectors; otherwise the entries come from L2
+      bool msm = false;
+      if constexpr (!BWD) {
+        msm = p.m_bulk != 0;
+        if (msm) wait_bar(bar_m, 0, abort_flag, (kRoleEpilogue << 8) | kBarM);
+      }
       if (BWD && p.stacked) {
         // stacked A: lane m < 64 holds M^T_hi row m, lane 64 + h holds M^T_lo row h
         const MixLine col(p, m & 63, false);
@@ -444,10 +463,30 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
         for (int i = 0; i < 2; ++i) {
           const int kh = i ^ kfirst;
           float v[64];
+          if (msm) {
+            // nh % 64 == 0: this half lies wholly inside or outside the block
+            const int o0 = kh * 64 - pb;  // first column of this half within the block
+            if (live && o0 >= 0 && o0 < p.nh) {
+              const float4* src =
+                  reinterpret_cast<const float4*>(gbase + C::kOffOut) + ((m - pb) * p.nh + o0) / 4;
 #pragma unroll
-          for (int q = 0; q < 64; ++q) {
-            const unsigned o = static_cast<unsigned>(kh * 64 + q - pb);
-            v[q] = (live && o < static_cast<unsigned>(p.nh)) ? line.at(static_cast<int>(o)) : 0.f;
+              for (int u = 0; u < 16; ++u) {
+                const float4 t = src[u];
+                v[4 * u] = t.x;
+                v[4 * u + 1] = t.y;
+                v[4 * u + 2] = t.z;
+                v[4 * u + 3] = t.w;
+              }
+            } else {
+#pragma unroll
+              for (int q = 0; q < 64; ++q) v[q] = 0.f;
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 64; ++q) {
+              const unsigned o = static_cast<unsigned>(kh * 64 + q - pb);
+              v[q] = (live && o < static_cast<unsigned>(p.nh)) ? line.at(static_cast<int>(o)) : 0.f;
+            }
           }
           uint32_t whi[32], wlo[32];
 #pragma unroll
@@ -1053,6 +1092,15 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
   }
 
   // ------------------------------------------------------------ teardown
+  // M's bulk copy must have landed before the CTA leaves (it has, unless the
+  // CTA gave up early): bounded wait that ignores the abort flag
+  if constexpr (!BWD) {
+    if (p.m_bulk && threadIdx.x == 0 && !ptx::mbar_try_wait(bar_m, 0)) {
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (!ptx::mbar_try_wait(bar_m, 0) && ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+  }
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -1252,6 +1300,8 @@ extern "C" int invrope_postmix_fwd_ex(const void* O, const float* M, void* Y, in
   p.n_ct = s.n_ct;
   p.pos = positions;
   p.gs = gs;
+  // M by one bulk copy at kernel start: 16-byte aligned, ungrouped, nh % 64 == 0
+  p.m_bulk = (aligned(M, 16) && gs == nh && nh % 64 == 0) ? 1 : 0;
   fill_freq(p.F, pe, theta);
   const int64_t grid = s.n_tiles < dev.sms ? s.n_tiles : dev.sms;
   postmix_kernel<false><<<static_cast<unsigned>(grid), KCfg<false>::kThreads, KCfg<false>::kSmemAlloc,
@@ -1330,6 +1380,7 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
     p.stacked = (!wide && nh == 64 && pe == kChunkCols && nope % kChunkCols == 0) ? 1 : 0;
     p.pos = positions;
     p.gs = gs;
+    p.m_bulk = 0;  // the backward reads M from L2 (a bulk copy did not pay off there)
     fill_freq(p.F, pe, theta);
     if (wide)
       postmix_kernel<true, true>
