@@ -177,3 +177,22 @@ def test_remap_i64_matches_int32_in_range():
     a = ir.kv_idx_local_to_global(idx, 1024, c.seqlen_kv)
     b = ir.kv_idx_local_to_global_i64(idx.to(torch.int64), 1024, c.seqlen_kv)
     assert torch.equal(a.to(torch.int64), b)
+
+
+# ------------------------------------------------------------------ M placement
+def test_forward_with_misaligned_M_matches_bitwise():
+    """An M that is only 4-byte aligned takes the forward's L2 path instead of
+    the bulk copy into shared memory; both give the same bits."""
+    sq, nh, nope, pe = 300, 64, 448, 64
+    O, dY = _inputs(sq, nh, nope + pe, seed=90)
+    M = W.postmix_M(nh, 91, "cuda")
+    flat = torch.empty(nh * nh + 1, dtype=torch.float32, device="cuda")
+    M_off = flat[1:].view(nh, nh)
+    M_off.copy_(M)
+    assert M_off.data_ptr() % 16 != 0
+    a = ir.invrope_postmix_fwd(O, M, 7, nope, pe)
+    b = ir.invrope_postmix_fwd(O, M_off, 7, nope, pe)
+    assert torch.equal(a, b)
+    da = ir.invrope_postmix_bwd(dY, O, M, 7, nope, pe)
+    db = ir.invrope_postmix_bwd(dY, O, M_off, 7, nope, pe)
+    assert torch.equal(da[0], db[0]) and torch.equal(da[1], db[1])
