@@ -14,7 +14,10 @@ import os
 
 import torch
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libinvrope.so")
+# INVROPE_LIBRARY selects another build of the same library (e.g. the
+# debug-bounds build, libinvrope_debug.so); it must export the same symbols.
+_LIB_PATH = os.environ.get("INVROPE_LIBRARY") or os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                                                             "libinvrope.so")
 _lib = None
 
 INVROPE_OK = 0

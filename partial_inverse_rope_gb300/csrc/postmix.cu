@@ -55,6 +55,22 @@ namespace invrope {
 
 __device__ unsigned int g_fault_code = 0;
 
+// Debug-bounds builds (-DINVROPE_DEBUG_BOUNDS, see build.py --debug-bounds)
+// check index invariants on the device and record 0xDB00 | id in the fault
+// code when one fails, without trapping (the access itself still happens, so
+// a check guards against silent corruption, not against a fault). In normal
+// builds the checks compile to nothing.
+#ifdef INVROPE_DEBUG_BOUNDS
+#define INVROPE_DBG_CHECK(cond, id)                              \
+  do {                                                           \
+    if (!(cond)) atomicCAS(&g_fault_code, 0u, 0xDB00u | (id));   \
+  } while (0)
+#else
+#define INVROPE_DBG_CHECK(cond, id) \
+  do {                              \
+  } while (0)
+#endif
+
 // Dynamic tile scheduling of the forward: one {next tile, finished CTAs} pair
 // per launch slot. A launch takes slot (launch sequence number mod
 // kSchedSlots); its last CTA returns the pair to zero.
@@ -253,6 +269,7 @@ __device__ __forceinline__ void fill_rot_table(float2* tab, const uint64_t* F, c
 
 // byte address of the 16-byte unit holding channel `col` (tile-relative) of row r
 __device__ __forceinline__ uint32_t swz_unit_addr(uint32_t tile, int r, int col) {
+  INVROPE_DBG_CHECK(r >= 0 && r < kRowsMax && col >= 0 && col < 2 * kChunkCols, 1);
   const int chunk = col >> 6;
   const int unit = (col & 63) >> 3;
   return tile + chunk * kChunkBytes + r * 128 + ((unit ^ (r & 7)) << 4);
@@ -535,6 +552,9 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
           stage_tile[st] = static_cast<int>(t);
         }
         const Tile x = decode_tile<BWD, WIDE>(p, t);
+        INVROPE_DBG_CHECK(t >= 0 && t < p.n_tiles && x.row0 >= 0 && x.c0 % kChunkCols == 0 && x.c0 < p.d &&
+                              x.nch >= 1 && x.nch <= C::kChunks,
+                          2);
         const uint32_t bytes = static_cast<uint32_t>(x.nch * p.R * 128 * (BWD ? 2 : 1));
         ptx::mbar_arrive_expect_tx(bar_full(st), bytes);
         const uint32_t sa = stage_addr(st);
@@ -606,6 +626,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
           break;
         }
         const Tile x = decode_tile<BWD, WIDE>(p, t);
+        INVROPE_DBG_CHECK(st < S && acc < NA && t >= 0 && t < p.n_tiles, 3);
         // The transform warps only see pe tiles; this thread has observed every
         // stage phase in order, so it tells them when the pe tile has landed.
         if (BWD && x.has_pe) ptx::mbar_arrive(bar_x_go);
@@ -720,6 +741,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
         ptx::named_bar_sync(1, 128);
       }
       const uint32_t taddr = tmem_base + lane_addr + static_cast<uint32_t>(acc) * acc_cols;
+      INVROPE_DBG_CHECK((static_cast<uint32_t>(acc) + 1u) * acc_cols <= static_cast<uint32_t>(C::kD2Col), 4);
       for (int k = 0; k < x.nch; ++k, ++n) {
         const int b = static_cast<int>(n % OB);
         if (!stk && !group_wait(bar_ob_empty(b), ((n / OB) & 1u) ^ 1u, abort_flag,
@@ -995,6 +1017,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
           }
           const int k = BWD ? kk : ob_chunk[b];
           const Tile x = decode_tile<BWD, WIDE>(p, t);
+          INVROPE_DBG_CHECK(b < OB && k < x.nch && x.c0 + k * kChunkCols < p.d, 6);
           ptx::tma_store_2d(&p.tm_out, out_addr(b), x.c0 + k * kChunkCols, x.row0);
           ptx::bulk_commit();
           // keep kIn stores reading; recycle the buffer of the oldest finished one
@@ -1034,6 +1057,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
         ptx::named_bar_sync(2, 128);
         if (xr < p.R) {
           const int kpe = (p.nope - x.c0) / kChunkCols;
+          INVROPE_DBG_CHECK(kpe >= 0 && kpe < x.nch && st < S, 5);
           const uint32_t oc = stage_addr(st) + C::kTensorTile + kpe * kChunkBytes;
           const uint32_t xl = base + C::kOffXlo;
           const int pc = p.nope - (x.c0 + kpe * kChunkCols);
