@@ -629,7 +629,12 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
         INVROPE_DBG_CHECK(st < S && acc < NA && t >= 0 && t < p.n_tiles, 3);
         // The transform warps only see pe tiles; this thread has observed every
         // stage phase in order, so it tells them when the pe tile has landed.
-        if (BWD && x.has_pe) ptx::mbar_arrive(bar_x_go);
+        // They take one hand-off at a time: when every tile is a pe tile (one
+        // channel tile) the previous one is still pending here, and this tile
+        // is handed over only after that one's flush below (its X used), so two
+        // hand-offs never complete on bar_x_go before they have seen the first.
+        const bool handoff_early = BWD && x.has_pe && pend_st < 0;
+        if (handoff_early) ptx::mbar_arrive(bar_x_go);
         if (!wait_bar(bar_acc_empty(acc), aph ^ 1u, abort_flag, (kRoleMma << 8) | kBarAccEmpty)) break;
         ptx::tc_fence_after();
         const uint32_t sa = stage_addr(st);
@@ -667,6 +672,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
           ptx::tc_commit(bar_empty(st));
         }
         if (pend_st >= 0 && !flush_pending()) break;
+        if (x.has_pe && !handoff_early) ptx::mbar_arrive(bar_x_go);
         if (x.has_pe) {
           pend_st = st;
           pend_x = x;

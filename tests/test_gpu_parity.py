@@ -178,6 +178,27 @@ def test_bitwise_repeatable():
         assert torch.equal(dM, outs[0][2])
 
 
+@pytest.mark.parametrize("nh,nope,pe", [(64, 0, 64), (16, 0, 32), (64, 8, 56)])
+def test_every_tile_a_pe_tile_repeated(nh, nope, pe):
+    """One channel tile, so every backward tile carries pe channels and the
+    hand-offs to the transform warps come back to back; many calls in a row
+    must all finish (no wait runs out) with bitwise identical results."""
+    sq = 8192
+    O, dY, M = make_inputs(sq, nh, nope, pe, seed=12)
+    dO0, dM0 = ir.invrope_postmix_bwd(dY, O, M, 3, nope, pe)
+    for _ in range(12):
+        dO, dM = ir.invrope_postmix_bwd(dY, O, M, 3, nope, pe)
+        assert torch.equal(dO, dO0)
+        assert torch.equal(dM, dM0)
+    torch.cuda.synchronize()
+    assert ir.invrope_take_device_fault() == 0
+    rows = sample_rows(sq, 128 // nh, 16)
+    dO_ref, _ = oracle.postmix_bwd(f64(dY[rows]), f64(O[rows]), f64(M), 3 + rows, nope, pe, 1e4)
+    assert_bf16_close(f64(dO0[rows]), dO_ref, "dO")
+    dM_ref = oracle.postmix_bwd_dM(f64(dY), f64(O), np.arange(3, 3 + sq, dtype=np.int64), nope, pe, 1e4)
+    assert_dm_close(f64(dM0), dM_ref)
+
+
 def test_bwd_with_no_rows_zeroes_dM():
     O = torch.empty(0, 4, 64, dtype=torch.bfloat16, device="cuda")
     M = torch.eye(4, device="cuda")
