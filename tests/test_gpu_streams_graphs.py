@@ -1,0 +1,92 @@
+"""The library's calls on several streams at once, and inside a captured CUDA
+graph: both must give the same bits as plain calls on one stream. The forward
+claims tiles from a per-launch counter slot and the backward's reduction is a
+programmatic dependent launch, so these are the paths that concurrency and
+capture could disturb. Needs a GB300 (sm_103a)."""
+
+import pytest
+import torch
+
+import partial_inverse_rope_gb300 as ir
+from gpu_helpers import ensure_built, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+SHAPE = (2048, 16, 448, 64)  # sq, nh, nope, pe (the mid config's shape)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    ensure_built()
+    yield
+    assert ir.invrope_take_device_fault() == 0, "a kernel wait ran out during the tests"
+
+
+def _case(seed):
+    sq, nh, nope, pe = SHAPE
+    O, dY, M = make_inputs(sq, nh, nope, pe, seed=seed)
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    idx = torch.randint(-1, 4096, (4 * 512, 256), generator=g, device="cuda", dtype=torch.int32)
+    return O, dY, M, idx
+
+
+def _outputs(O, idx):
+    nh = O.shape[1]
+    ws = torch.empty(ir.invrope_postmix_bwd_workspace_bytes(*SHAPE), dtype=torch.uint8, device="cuda")
+    return dict(Y=torch.empty_like(O), dO=torch.empty_like(O),
+                dM=torch.empty(nh, nh, dtype=torch.float32, device="cuda"),
+                out=torch.empty_like(idx), ws=ws)
+
+
+def _run(case, o, stream=None):
+    O, dY, M, idx = case
+    _, _, nope, pe = SHAPE
+    ir.invrope_postmix_fwd(O, M, 7, nope, pe, Y=o["Y"], stream=stream)
+    ir.invrope_postmix_bwd(dY, O, M, 7, nope, pe, dO=o["dO"], dM=o["dM"], workspace=o["ws"], stream=stream)
+    ir.kv_idx_local_to_global(idx, 512, 4096, out=o["out"], stream=stream)
+
+
+def _same(a, b):
+    for k in ("Y", "dO", "dM", "out"):
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_concurrent_streams_match_one_stream():
+    cases = [_case(s) for s in (21, 22, 23)]
+    ref = []
+    for c in cases:
+        o = _outputs(c[0], c[3])
+        _run(c, o)
+        ref.append(o)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in cases]
+    outs = [_outputs(c[0], c[3]) for c in cases]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    for _ in range(3):
+        for c, o, s in zip(cases, outs, streams):
+            _run(c, o, stream=s)
+    torch.cuda.synchronize()
+    for r, o in zip(ref, outs):
+        _same(r, o)
+
+
+def test_graph_replay_matches_eager():
+    case = _case(31)
+    eager = _outputs(case[0], case[3])
+    _run(case, eager)  # also loads the module and sets kernel attributes before capture
+    torch.cuda.synchronize()
+    o = _outputs(case[0], case[3])
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            _run(case, o)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for v in o.values():
+            v.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        _same(eager, o)
