@@ -68,6 +68,10 @@ SHAPES = [
     (40, 128, 64, 64, 0, 1e4),        # d = 128: one 128-channel tile per row tile, every tile has pe
     (50, 96, 480, 32, 5, 1e4),        # 128-channel backward tiles, pe = 32 in the last 64-channel chunk
     (2053, 16, 448, 64, 0, 1e4),      # mid-like, ragged
+    (777, 32, 448, 64, 1, 1e4),       # nh = 32: 4 positions per tile
+    (515, 48, 448, 64, 2, 1e4),       # nh = 48: 2 positions, R = 96, block-diagonal backward mix
+    (200, 24, 100, 28, 4, 1e4),       # pe/2 = 14 (scalar rotation path), pe block inside chunk 1
+    (90, 128, 510, 2, 6, 1e4),        # 128 heads, the smallest pe (one pair) at the end of d = 512
 ]
 
 
