@@ -13,9 +13,11 @@ from .invrope_oracle import (  # noqa: F401
     rope,
     postmix_fwd,
     postmix_bwd,
+    postmix_bwd_dO,
     postmix_bwd_dM,
     postmix_fwd_grouped,
     postmix_bwd_grouped,
+    postmix_bwd_grouped_dO,
     kv_idx_local_to_global,
     kv_idx_local_to_global_i64,
     positions_contiguous,

@@ -152,18 +152,24 @@ def postmix_bwd_dM(dY, O, positions, nope: int, pe: int, theta: float,
     return dM
 
 
-def postmix_bwd(dY, O, M, positions, nope: int, pe: int, theta: float):
-    """Backward of :func:`postmix_fwd`: returns ``(dO, dM)`` in fp64.
+def postmix_bwd_dO(dY, M, positions, nope: int, pe: int, theta: float) -> np.ndarray:
+    """Input gradient of :func:`postmix_fwd` in fp64.
 
     ``dX[s, h, :] = sum_g M[g, h] dY[s, g, :]`` is the GEMM's input gradient
     and ``dO = rope(dX)`` on the pe channels (``dX`` on the nope channels)
     because the inverse rotation is orthogonal ([PR1772] revision note: the
     input gradient is the matmul backward of the unfused postmix, pushed
-    through the rotation). ``dM`` follows :func:`postmix_bwd_dM`.
+    through the rotation).
     """
     M = _f64(M)
     G = np.matmul(M.T[None, :, :], _f64(dY))
-    dO = rope(G, positions, nope, pe, theta)
+    return rope(G, positions, nope, pe, theta)
+
+
+def postmix_bwd(dY, O, M, positions, nope: int, pe: int, theta: float):
+    """Backward of :func:`postmix_fwd`: returns ``(dO, dM)`` in fp64, ``dO``
+    from :func:`postmix_bwd_dO` and ``dM`` from :func:`postmix_bwd_dM`."""
+    dO = postmix_bwd_dO(dY, M, positions, nope, pe, theta)
     dM = postmix_bwd_dM(dY, O, positions, nope, pe, theta)
     return dO, dM
 
@@ -211,13 +217,23 @@ def postmix_bwd_grouped(dY, O, Mg, positions, nope: int, pe: int, theta: float):
     ng, gs, _ = Mg.shape
     dY = np.asarray(dY)
     O = np.asarray(O)
-    G = np.empty(dY.shape, dtype=np.float64)
     dMg = np.empty((ng, gs, gs), dtype=np.float64)
     for k, sl in enumerate(_group_slices(dY.shape[1], gs)):
-        G[:, sl, :] = np.matmul(Mg[k].T[None, :, :], _f64(dY[:, sl, :]))
         dMg[k] = postmix_bwd_dM(dY[:, sl, :], O[:, sl, :], positions, nope, pe, theta)
-    dO = rope(G, positions, nope, pe, theta)
+    dO = postmix_bwd_grouped_dO(dY, Mg, positions, nope, pe, theta)
     return dO, dMg
+
+
+def postmix_bwd_grouped_dO(dY, Mg, positions, nope: int, pe: int, theta: float) -> np.ndarray:
+    """Input gradient of :func:`postmix_fwd_grouped` in fp64: per group ``k``,
+    ``dX = Mg[k]^T dY`` on the group's heads, rotated back by ``+a`` on the
+    pe channels (as in :func:`postmix_bwd_dO`)."""
+    Mg = _f64(Mg)
+    dY = np.asarray(dY)
+    G = np.empty(dY.shape, dtype=np.float64)
+    for k, sl in enumerate(_group_slices(dY.shape[1], Mg.shape[1])):
+        G[:, sl, :] = np.matmul(Mg[k].T[None, :, :], _f64(dY[:, sl, :]))
+    return rope(G, positions, nope, pe, theta)
 
 
 def kv_idx_local_to_global(idx, sq: int, seqlen_kv: int) -> np.ndarray:
@@ -281,7 +297,7 @@ def positions_contiguous(sq: int, pos0: int) -> np.ndarray:
 
 __all__ = [
     "inv_freq", "rope_angles", "invrope", "rope", "postmix_fwd",
-    "postmix_bwd", "postmix_bwd_dM", "postmix_fwd_grouped",
-    "postmix_bwd_grouped", "kv_idx_local_to_global",
+    "postmix_bwd", "postmix_bwd_dO", "postmix_bwd_dM", "postmix_fwd_grouped",
+    "postmix_bwd_grouped", "postmix_bwd_grouped_dO", "kv_idx_local_to_global",
     "kv_idx_local_to_global_i64", "positions_contiguous", "positions_batched",
 ]

@@ -16,8 +16,9 @@ forms, hand-derived integers, invariants and brute force):
 * forward definition: pure-Python brute force on a tiny case, the position-0
   and identity / permutation special cases, commutation of the head mix with
   the per-position rotation;
-* backward: the adjoint identity ``<fwd(O), dY> = <O, dO(dY)>``, dM from
-  unit matrices (``Y`` is linear in ``M``) and central finite differences;
+* backward: pure-Python brute force of dO (both the full backward and the
+  dO-only function), the adjoint identity ``<fwd(O), dY> = <O, dO(dY)>``, dM
+  from unit matrices (``Y`` is linear in ``M``) and central finite differences;
 * remap: the hand-derived ``golden/kv_remap_small.json`` and brute force;
   the int64 table the same, plus the 64-bit wrap;
 * grouped postmix: one group equals the ungrouped postmix, several groups
@@ -204,6 +205,7 @@ def check_bwd_brute_force_dO(impl):
             dO[s, :, nope + h + i] = g2 * math.cos(a) + g1 * math.sin(a)
     got, _ = impl.postmix_bwd(dY, O, M, pos, nope, pe, theta)
     _close(got, dO, what="brute force dO")
+    _close(impl.postmix_bwd_dO(dY, M, pos, nope, pe, theta), dO, what="brute force dO (dO only)")
 
 
 def check_adjoint_identity(impl):
@@ -348,9 +350,22 @@ def check_grouped_brute_force(impl):
                 Y[s, g, c] = sum(Mg[k, i, j] * X[s, k * gs + j, c] for j in range(gs))
                 for j in range(gs):
                     dM[k, i, j] += dY[s, g, c] * X[s, k * gs + j, c]
+    # dO: the group's transposed mix of dY, rotated back by +a (pe = 2: one pair)
+    dO = np.zeros_like(O)
+    for s in range(sq):
+        a = pos[s] * 1.0
+        for h in range(nh):
+            k, j = divmod(h, gs)
+            G = [sum(Mg[k, i, j] * dY[s, k * gs + i, c] for i in range(gs)) for c in range(d)]
+            dO[s, h, 0] = G[0]
+            dO[s, h, 1] = G[1] * math.cos(a) - G[2] * math.sin(a)
+            dO[s, h, 2] = G[2] * math.cos(a) + G[1] * math.sin(a)
     _close(impl.postmix_fwd_grouped(O, Mg, pos, nope, pe, theta), Y, what="brute force grouped Y")
-    _close(impl.postmix_bwd_grouped(dY, O, Mg, pos, nope, pe, theta)[1], dM,
-           what="brute force grouped dM")
+    got_dO, got_dM = impl.postmix_bwd_grouped(dY, O, Mg, pos, nope, pe, theta)
+    _close(got_dM, dM, what="brute force grouped dM")
+    _close(got_dO, dO, what="brute force grouped dO")
+    _close(impl.postmix_bwd_grouped_dO(dY, Mg, pos, nope, pe, theta), dO,
+           what="brute force grouped dO (dO only)")
 
 
 def check_positions_batched(impl):

@@ -71,16 +71,19 @@ def _postmix_ns(inv, fwd_rope, angles, mix_t=False, bwd_M=False, drop_nope=False
         dM = np.einsum("sgc,shc->gh", np.asarray(dY, dtype=np.float64), X)
         return dM.T if dM_t else dM
 
-    def postmix_bwd(dY, O, M, positions, nope, pe, theta):
+    def postmix_bwd_dO(dY, M, positions, nope, pe, theta):
         M = np.asarray(M, dtype=np.float64)
         G = np.matmul((M if bwd_M else M.T)[None], np.asarray(dY, dtype=np.float64))
         rot = fwd_rope if bwd_rot is None else bwd_rot
-        dO = rot(G, positions, nope, pe, theta)
+        return rot(G, positions, nope, pe, theta)
+
+    def postmix_bwd(dY, O, M, positions, nope, pe, theta):
+        dO = postmix_bwd_dO(dY, M, positions, nope, pe, theta)
         return dO, postmix_bwd_dM(dY, O, positions, nope, pe, theta)
 
     return _namespace(invrope=inv, rope=fwd_rope, rope_angles=angles,
                       postmix_fwd=postmix_fwd, postmix_bwd=postmix_bwd,
-                      postmix_bwd_dM=postmix_bwd_dM)
+                      postmix_bwd_dO=postmix_bwd_dO, postmix_bwd_dM=postmix_bwd_dM)
 
 
 def _mutants():
@@ -115,7 +118,7 @@ def _mutants():
         out = np.where(idx >= 0, idx + b * seqlen_kv, idx)
         return np.clip(out, -2**31, 2**31 - 1).astype(np.int32)
 
-    def grouped_ns(transpose_fwd=False, strided=False, dM_t=False):
+    def grouped_ns(transpose_fwd=False, strided=False, dM_t=False, dO_mix_untransposed=False):
         def groups(nh, gs):
             ng = nh // gs
             if strided:  # heads k, k+ng, k+2ng, ... instead of consecutive heads
@@ -131,19 +134,26 @@ def _mutants():
                 Y[:, hs, :] = np.matmul(m[None], X[:, hs, :])
             return Y
 
+        def bwd_dO(dY, Mg, positions, nope, pe, theta):
+            Mg = np.asarray(Mg, dtype=np.float64)
+            dY = np.asarray(dY, dtype=np.float64)
+            G = np.empty_like(dY)
+            for k, hs in enumerate(groups(dY.shape[1], Mg.shape[1])):
+                m = Mg[k] if dO_mix_untransposed else Mg[k].T
+                G[:, hs, :] = np.matmul(m[None], dY[:, hs, :])
+            return base.rope(G, positions, nope, pe, theta)
+
         def bwd(dY, O, Mg, positions, nope, pe, theta):
             Mg = np.asarray(Mg, dtype=np.float64)
             dY = np.asarray(dY, dtype=np.float64)
             X = base.invrope(O, positions, nope, pe, theta)
-            G = np.empty_like(dY)
             dM = np.empty_like(Mg)
             for k, hs in enumerate(groups(dY.shape[1], Mg.shape[1])):
-                G[:, hs, :] = np.matmul(Mg[k].T[None], dY[:, hs, :])
                 blk = np.einsum("sgc,shc->gh", dY[:, hs, :], X[:, hs, :])
                 dM[k] = blk.T if dM_t else blk
-            return base.rope(G, positions, nope, pe, theta), dM
+            return bwd_dO(dY, Mg, positions, nope, pe, theta), dM
 
-        return _namespace(postmix_fwd_grouped=fwd, postmix_bwd_grouped=bwd)
+        return _namespace(postmix_fwd_grouped=fwd, postmix_bwd_grouped=bwd, postmix_bwd_grouped_dO=bwd_dO)
 
     def remap64_by_row(idx, sq, seqlen_kv):
         idx = np.asarray(idx).astype(np.int64)
@@ -163,6 +173,7 @@ def _mutants():
         "grouped_blocks_transposed": grouped_ns(transpose_fwd=True),
         "grouped_heads_strided": grouped_ns(strided=True),
         "grouped_dM_transposed": grouped_ns(dM_t=True),
+        "grouped_dO_mix_untransposed": grouped_ns(dO_mix_untransposed=True),
         "remap64_offset_by_row": _namespace(kv_idx_local_to_global_i64=remap64_by_row),
         "remap64_saturates": _namespace(kv_idx_local_to_global_i64=remap64_saturates),
         "remap64_truncates_to_int32": _namespace(kv_idx_local_to_global_i64=remap64_via_int32),
