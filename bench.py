@@ -18,7 +18,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -35,8 +34,10 @@ from partial_inverse_rope_gb300 import inputs as W  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["partial_inverse_rope_gb300/csrc/postmix.cu",
-                  "partial_inverse_rope_gb300/csrc/ptx.cuh"]
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "postmix_bwd_production_shard.md")
+                  "partial_inverse_rope_gb300/csrc/ptx.cuh",
+                  "partial_inverse_rope_gb300/csrc/sched.cuh"]
+# machine-readable ncu counters of the backward kernel (written beside its summary)
+PROFILE_COUNTERS = os.path.join(ROOT, "profiles", "postmix_bwd_production_shard.json")
 
 
 # ---------------------------------------------------------------- environment
@@ -66,17 +67,16 @@ def kernel_source_hash():
 
 def profiled_traffic():
     """Per-launch DRAM bytes of the backward kernel from the committed ncu
-    summary, or None when the summary is missing or predates the current
+    counters (JSON), or None when they are missing or were taken with another
     kernel source."""
     try:
-        text = open(PROFILE_SUMMARY).read()
-    except OSError:
+        with open(PROFILE_COUNTERS) as f:
+            rec = json.load(f)
+        if rec["kernel_source_sha256_16"] != kernel_source_hash():
+            return None
+        return int(rec["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError, TypeError):
         return None
-    src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    traffic = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
-    if not src or not traffic or src.group(1) != kernel_source_hash():
-        return None
-    return int(traffic.group(1))
 
 
 class ClockSampler:
@@ -219,6 +219,7 @@ def run_ours(args, rank, world, local):
     e2e = run_e2e(args, ir, c, R, dev, stream, O, dY, Ms, idx, Y, dO, dM, ws, out, world)
 
     peak, peak_kind = measured_peak()
+    configs = config_sweep(ir, dev, stream, peak) if rank == 0 else None
     bwd_avg = statistics.mean(bwd_us)
     achieved = c.bwd_bytes() / (bwd_avg * 1e-6) / 1e9
     line = {
@@ -272,8 +273,83 @@ def run_ours(args, rank, world, local):
         "device_fault": fault,
     }
     if rank == 0:
-        line["cpu_baseline"] = cpu_baseline(args)
+        base = cpu_baseline(args)
+        line["cpu_baseline"] = base
+        # the production shard's oracle time per config line: the cpu_baseline run itself
+        prod = configs[W.PROD.name]["oracle"]
+        prod.update({"rows": base["rows"], "fwd_bwd_s": base["postmix_s"], "cores": base["cores"]})
+        prod["gbs"] = round((W.PROD.fwd_bytes() + W.PROD.bwd_bytes()) * base["rows"] / W.PROD.sq
+                            / base["postmix_s"] / 1e9, 3)
+        line["configs"] = configs
         print(json.dumps(line), flush=True)
+
+
+# rows of each config the oracle runs in the per-config sweep (the rest scale)
+CONFIG_ORACLE_ROWS = {"tiny": 128, "mid": 2048, "sweep_nh3": 8192, "sweep_nh128": 2048}
+
+
+def config_sweep(ir, dev, stream, peak):
+    """Every postmix config: forward and backward timed alone with CUDA events
+    (median of 20 calls, a 512 MiB buffer rewritten before each so that no
+    input is served from the 129 MB L2), algorithmic GB/s and the fraction of
+    the measured copy peak; beside it the fp64 oracle's time for fwd + bwd on
+    the host cores (all rows, or a leading block of rows scaled to the config;
+    the production shard's oracle time is the cpu_baseline run)."""
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    res = {}
+    for c in (W.TINY, W.MID, W.SWEEP_NH3, W.SWEEP_NH128, W.PROD):
+        O, dY, M = W.postmix_inputs(c, device=dev)
+        Y, dO = torch.empty_like(O), torch.empty_like(O)
+        dM = torch.empty(c.nh, c.nh, dtype=torch.float32, device=dev)
+        ws = torch.empty(max(16, ir.invrope_postmix_bwd_workspace_bytes(c.sq, c.nh, c.nope, c.pe)),
+                         dtype=torch.uint8, device=dev)
+        calls = {
+            "fwd": lambda: ir.invrope_postmix_fwd(O, M, c.pos0, c.nope, c.pe, c.theta, Y=Y),
+            "bwd": lambda: ir.invrope_postmix_bwd(dY, O, M, c.pos0, c.nope, c.pe, c.theta, dO=dO, dM=dM,
+                                                  workspace=ws),
+        }
+        nbytes = {"fwd": c.fwd_bytes(), "bwd": c.bwd_bytes()}
+        row = {"shape": [c.sq, c.nh, c.nope, c.pe], "pos0": c.pos0}
+        for name, fn in calls.items():
+            for _ in range(3):
+                fn()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+            for e0, e1 in ev:
+                flush.fill_(1)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            us = statistics.median(e0.elapsed_time(e1) * 1e3 for e0, e1 in ev)
+            gbs = nbytes[name] / (us * 1e-6) / 1e9
+            row[f"{name}_us"] = round(us, 2)
+            row[f"{name}_gbs"] = round(gbs, 1)
+            row[f"{name}_frac"] = round(gbs / peak, 4)
+        del O, dY, Y, dO, ws
+        row["oracle"] = oracle_config(c) if c.name in CONFIG_ORACLE_ROWS else {"kind": "oracle"}
+        res[c.name] = row
+    del flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def oracle_config(c):
+    """fp64 oracle fwd + bwd (dO, dM) on the first rows of config `c`."""
+    import numpy as np
+
+    import oracle
+
+    rows = min(c.sq, CONFIG_ORACLE_ROWS[c.name])
+    sub = W.PostmixConfig(c.name, sq=rows, nh=c.nh, nope=c.nope, pe=c.pe, pos0=c.pos0, seed=c.seed)
+    O, dY, M = W.postmix_inputs(sub, device="cpu")
+    O64, dY64, M64 = (t.to(torch.float64).numpy() for t in (O, dY, M))
+    pos = np.arange(c.pos0, c.pos0 + rows, dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.postmix_fwd(O64, M64, pos, c.nope, c.pe, c.theta)
+    oracle.postmix_bwd(dY64, O64, M64, pos, c.nope, c.pe, c.theta)
+    dt = time.perf_counter() - t0
+    return {"kind": "oracle", "rows": rows, "fwd_bwd_s": round(dt, 4), "cores": oracle_threads(),
+            "gbs": round((c.fwd_bytes() + c.bwd_bytes()) * rows / c.sq / dt / 1e9, 3)}
 
 
 def run_e2e(args, ir, c, R, dev, stream, O, dY, Ms, idx, Y, dO, dM, ws, out, world):
@@ -400,11 +476,12 @@ def oracle_sample(rows: int, threads_note=True):
     t0 = time.perf_counter()
     oracle.postmix_fwd(O64, M64, pos, c.nope, c.pe, c.theta)
     oracle.postmix_bwd(dY64, O64, M64, pos, c.nope, c.pe, c.theta)
+    t1 = time.perf_counter()
     oracle.kv_idx_local_to_global(idx_np, R.sq, R.seqlen_kv)
     dt = time.perf_counter() - t0
     nbytes = (2 * rows * c.nh * c.d * 2 + 4 * c.nh * c.nh) + (3 * rows * c.nh * c.d * 2 + 8 * c.nh * c.nh) \
         + 2 * idx.numel() * 4
-    return dt, nbytes, rows, idx.shape[0]
+    return dt, nbytes, rows, idx.shape[0], t1 - t0
 
 
 def oracle_threads():
@@ -420,9 +497,9 @@ def oracle_threads():
 
 def cpu_baseline(args):
     rows = int(os.environ.get("INVROPE_ORACLE_ROWS", "16384"))
-    dt, nbytes, rows, idx_rows = oracle_sample(rows)
+    dt, nbytes, rows, idx_rows, postmix_s = oracle_sample(rows)
     return {"value": round(nbytes / dt / 1e9, 3), "unit": "GB/s", "cores": oracle_threads(),
-            "kind": "oracle",
+            "kind": "oracle", "rows": rows, "postmix_s": round(postmix_s, 3),
             "sample": f"fp64 numpy oracle: fwd+bwd(dO, dM) on the first {rows} of 16384 positions "
                       f"of the production shard + remap of {idx_rows} table rows; "
                       f"{dt:.2f} s wall, scaled to algorithmic GB/s"}
@@ -437,7 +514,7 @@ def run_reference(args, rank, world):
     for _ in range(args.warmup):
         oracle_sample(rows)
     for _ in range(args.steps):
-        dt, nbytes, rows, idx_rows = oracle_sample(rows)
+        dt, nbytes, rows, idx_rows, _ = oracle_sample(rows)
         times.append(dt)
     sec = statistics.mean(times)
     value = nbytes / sec / 1e9

@@ -31,14 +31,25 @@
  *
  * Common contract of every call below:
  *   - Pointers are DEVICE pointers of the current CUDA device, owned by the
- *     caller. The library allocates no device memory at call time and keeps
- *     no state between calls beyond cached device attributes, loaded kernels
- *     and two small per-device arrays of work counters (2 KB for the
- *     forward's tiles, 4 KB for the remap's chunks): those kernels hand out
- *     their work dynamically (thread blocks claim the next tile or chunk from
- *     a counter), and the last thread block of a launch returns its counter
- *     to zero. A launch takes one of 256 counters in turn, so at most 256
- *     such launches may run at once per device.
+ *     caller. The library allocates no device memory at call time. Between
+ *     calls it keeps cached device attributes and host-side caches, its
+ *     loaded kernels, and library-owned device arrays that exist from module
+ *     load until the process exits:
+ *       . two arrays of 512 work-counter slots (8 KB each) for the forward
+ *         and the remap, which hand out their work dynamically (thread blocks
+ *         claim the next tile or chunk from their launch's slot);
+ *       . the 8 MiB scratch array of invrope_postmix_bwd_noalloc (see there
+ *         for how calls share it and must be ordered).
+ *     Work-counter slots: an eager launch takes the next of 256 slots in
+ *     turn, a launch made while its stream is being captured into a CUDA
+ *     graph the next of 256 other slots, which it keeps on every replay. A
+ *     launch's thread blocks take their slot only when it is free or held by
+ *     their own launch; the last block frees it. A launch that finds its
+ *     slot held by another launch still running (more than 256 eager
+ *     launches in flight at once, or two concurrent replays of captured
+ *     launches that share a slot) claims nothing from it, records
+ *     INVROPE_FAULT_SCHED_BUSY_FWD or _REMAP (see invrope_take_device_fault)
+ *     and leaves its outputs undefined; it never disturbs the other launch.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream). Every call
  *     only enqueues work on `stream` and returns; nothing synchronises.
  *   - Arguments are validated on the host before anything is enqueued; a
@@ -256,12 +267,30 @@ int kv_idx_local_to_global_i64(const int64_t* idx, int64_t* out,
                                int64_t seqlen_kv, struct CUstream_st* stream);
 
 /*
- * Synchronises the current device, then returns in *fault the watchdog code
+ * Synchronises the current device, then returns in *fault the fault code
  * recorded by any kernel of this library on this device since the previous
  * call (0 = none) and clears it. A non-zero code means a bounded wait ran
- * out and that launch's outputs are undefined.
+ * out (code = role << 8 | barrier), or a launch found its work-counter slot
+ * held by another launch (INVROPE_FAULT_SCHED_BUSY_*); the outputs of the
+ * launches since the previous call are then undefined. After a non-zero code
+ * every work-counter slot of the device is returned to the free state (no
+ * call of this library may be running on the device at that point).
  */
+#define INVROPE_FAULT_SCHED_BUSY_FWD 0x5C1
+#define INVROPE_FAULT_SCHED_BUSY_REMAP 0x5C2
 int invrope_take_device_fault(int* fault);
+
+/*
+ * Test hook (library infrastructure, not an operation of the pages): marks
+ * the work-counter slot that the next eager forward (which = 0) or KV remap
+ * (which = 1) launch on the current device will take as held by the launch
+ * tag `owner` (a synchronous host-to-device copy). With a non-zero owner
+ * that no launch has, that next launch must find the slot busy, record
+ * INVROPE_FAULT_SCHED_BUSY_FWD / _REMAP and leave its output undefined;
+ * invrope_take_device_fault() then frees the slot again. Lets a test check
+ * the collision path without running two launches at once.
+ */
+int invrope_debug_occupy_next_slot(int which, unsigned long long owner);
 
 /*
  * Watchdog self-test: launches one thread block whose only mbarrier wait can

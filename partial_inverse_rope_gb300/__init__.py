@@ -5,6 +5,7 @@ C ABI (``include/invrope.h``), with a thin ctypes binding of the same names.
 
 from .binding import (  # noqa: F401
     InvropeError,
+    invrope_debug_occupy_next_slot,
     invrope_postmix_bwd,
     invrope_postmix_bwd_ex,
     invrope_postmix_bwd_noalloc,

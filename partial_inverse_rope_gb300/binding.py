@@ -66,9 +66,12 @@ _SIGNATURES = {
         ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),
     "invrope_take_device_fault": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int)]),
     "invrope_watchdog_selftest": (ctypes.c_int, [ctypes.c_int64, ctypes.POINTER(ctypes.c_int)]),
+    "invrope_debug_occupy_next_slot": (ctypes.c_int, [ctypes.c_int, ctypes.c_ulonglong]),
 }
 
 INVROPE_WATCHDOG_SELFTEST_CODE = 0x60A
+INVROPE_FAULT_SCHED_BUSY_FWD = 0x5C1
+INVROPE_FAULT_SCHED_BUSY_REMAP = 0x5C2
 
 
 class InvropeError(RuntimeError):
@@ -306,6 +309,13 @@ def invrope_take_device_fault() -> int:
     v = ctypes.c_int(0)
     _check(lib().invrope_take_device_fault(ctypes.byref(v)), "invrope_take_device_fault")
     return v.value
+
+
+def invrope_debug_occupy_next_slot(which: str, owner: int) -> None:
+    """Test hook: mark the work-counter slot the next eager ``"fwd"`` or
+    ``"remap"`` launch will take as held by launch tag ``owner``."""
+    code = {"fwd": 0, "remap": 1}[which]
+    _check(lib().invrope_debug_occupy_next_slot(code, int(owner)), "invrope_debug_occupy_next_slot")
 
 
 def invrope_watchdog_selftest(limit_us: int = 50000) -> int:

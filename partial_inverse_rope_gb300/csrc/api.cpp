@@ -1,4 +1,5 @@
-// Status strings, error bookkeeping and the device-attribute cache of the C ABI.
+// Status strings, error bookkeeping, the device-attribute cache and the
+// host-side work-counter slot hand-out of the C ABI.
 #include <mutex>
 
 #include "common.h"
@@ -46,6 +47,50 @@ int current_device(DeviceInfo* out) {
   return INVROPE_OK;
 }
 
+namespace {
+int slot_base(SlotRing& ring, const void* symbol, int device) {
+  if (device < 0 || device >= 64) return INVROPE_ERR_DEVICE;
+  if (!ring.base[device]) {
+    void* ptr = nullptr;
+    const cudaError_t err = cudaGetSymbolAddress(&ptr, symbol);
+    if (err != cudaSuccess) return cuda_fail(err);
+    ring.base[device] = static_cast<SchedSlot*>(ptr);
+  }
+  return INVROPE_OK;
+}
+}  // namespace
+
+int slot_take(SlotRing& ring, const void* symbol, int device, cudaStream_t stream, SchedSlot** out) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  const cudaError_t err = cudaStreamIsCapturing(stream, &cap);
+  if (err != cudaSuccess) return cuda_fail(err);
+  std::lock_guard<std::mutex> lock(ring.mu);
+  const int st = slot_base(ring, symbol, device);
+  if (st != INVROPE_OK) return st;
+  if (cap == cudaStreamCaptureStatusNone)
+    *out = ring.base[device] + (ring.eager[device]++ % kEagerSlots);
+  else
+    *out = ring.base[device] + kEagerSlots + (ring.capture[device]++ % kCaptureSlots);
+  return INVROPE_OK;
+}
+
+int slot_peek_eager(SlotRing& ring, const void* symbol, int device, SchedSlot** out) {
+  std::lock_guard<std::mutex> lock(ring.mu);
+  const int st = slot_base(ring, symbol, device);
+  if (st != INVROPE_OK) return st;
+  *out = ring.base[device] + (ring.eager[device] % kEagerSlots);
+  return INVROPE_OK;
+}
+
+int slot_reset_all(SlotRing& ring, const void* symbol, int device) {
+  std::lock_guard<std::mutex> lock(ring.mu);
+  const int st = slot_base(ring, symbol, device);
+  if (st != INVROPE_OK) return st;
+  const cudaError_t err = cudaMemset(ring.base[device], 0, sizeof(SchedSlot) * kSchedSlots);
+  if (err != cudaSuccess) return cuda_fail(err);
+  return INVROPE_OK;
+}
+
 }  // namespace invrope
 
 extern "C" {
@@ -63,5 +108,14 @@ const char* invrope_status_string(int status) {
 }
 
 int invrope_last_cuda_error(void) { return invrope::g_last_cuda_error; }
+
+int invrope_debug_occupy_next_slot(int which, unsigned long long owner) {
+  int dev = 0;
+  const cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return invrope::cuda_fail(err);
+  if (which == 0) return invrope::occupy_postmix_slot(dev, owner);
+  if (which == 1) return invrope::occupy_remap_slot(dev, owner);
+  return INVROPE_ERR_INVALID_ARG;
+}
 
 }  // extern "C"

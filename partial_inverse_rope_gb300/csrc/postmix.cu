@@ -50,6 +50,7 @@
 
 #include "common.h"
 #include "ptx.cuh"
+#include "sched.cuh"
 
 namespace invrope {
 
@@ -71,11 +72,10 @@ __device__ unsigned int g_fault_code = 0;
   } while (0)
 #endif
 
-// Dynamic tile scheduling of the forward: one {next tile, finished CTAs} pair
-// per launch slot. A launch takes slot (launch sequence number mod
-// kSchedSlots); its last CTA returns the pair to zero.
-constexpr int kSchedSlots = 256;
-__device__ unsigned int g_sched[kSchedSlots][2];
+// Dynamic tile scheduling of the forward: one work-counter slot per launch
+// (sched.cuh): the first tile of a CTA is its block index, later ones are
+// claimed from the slot's counter.
+__device__ SchedSlot g_sched[kSchedSlots];
 
 namespace {
 
@@ -114,7 +114,7 @@ struct KCfg {
   static constexpr int kOffStage = 0;
   static constexpr int kOffOut = kOffStage + kStages * kStageBytes;
   static constexpr int kOffXlo = kOffOut + kOutBufs * kChunkBytes;
-  static constexpr int kXloBytes = BWD ? kChunkBytes : 0;
+  static constexpr int kXloBytes = BWD ? kChunks * kChunkBytes : 0;
   // bwd, stacked mix: fp32 exchange rows between the epilogue warp pairs (64 x 256 B)
   static constexpr int kOffXch = kOffXlo + kXloBytes;
   static constexpr int kXchBytes = (BWD && !WIDE) ? 64 * 256 : 0;
@@ -135,12 +135,15 @@ struct KCfg {
 };
 
 struct PostmixParams {
-  CUtensorMap tm_in0;  // fwd: O      bwd: dY
-  CUtensorMap tm_in1;  // bwd: O
-  CUtensorMap tm_out;  // fwd: Y      bwd: dO
+  CUtensorMap tm_in0;  // fwd: O      bwd: dY   (general tiling: clipped at channel nope)
+  CUtensorMap tm_in1;  // bwd: O                (general tiling: clipped at channel nope)
+  CUtensorMap tm_out;  // fwd: Y      bwd: dO   (general tiling: clipped at channel nope)
+  CUtensorMap tm_in0_pe;  // general tiling, pe tiles: in0 over all d channels
+  CUtensorMap tm_in1_pe;  // general tiling, pe tiles: in1 over all d channels
+  uint16_t* out;       // Y or dO (bf16 bits): the general tiling's pe tiles store directly
   const float* M;
   float* ws;           // bwd: per-CTA dM partials [gridDim.x][nh][nh]
-  unsigned int* sched; // fwd: this launch's {next tile, finished CTAs} counters
+  SchedSlot* sched;    // fwd: this launch's work-counter slot
   uint64_t F[kMaxHalf];  // rotary frequencies in turns per position, 0.64 fixed point
   int64_t sq;
   int64_t pos0;
@@ -153,13 +156,32 @@ struct PostmixParams {
   const int32_t* pos;  // per-row positions (pos0 is added), or null: row s sits at pos0 + s
   int gs;              // heads per group of the head mix (nh: one [nh, nh] matrix)
   int m_bulk;          // forward: M is copied into shared memory by one bulk copy at start
+  // General tiling (the pe block does not lie inside one 64-channel box): channel
+  // tiles [0, n_nope_ct) cover channels [0, nope & ~7) through the clipped maps;
+  // tile n_nope_ct + j is pair block j, rotation pairs [32 j, 32 j + 32) of the
+  // pe block, loaded as two boxes (first and second halves of its pairs).
+  int gen;
+  int n_nope_ct;
+  int64_t rows;        // sq * nh: rows of the [sq*nh, d] view
+  double log2_theta;   // rotary frequencies beyond the first 32 pairs are formed on the device
 };
 
+// kind 0: a tile of the regular tiling (channels c0 + 64 k, TMA-stored);
+// kind 1: a nope tile of the general tiling: channels [0, nope & ~7) through
+//   the maps clipped there (a clip on a 16-byte boundary), TMA-stored;
+// kind 2: a pair block of the general tiling: box 0 at channel xa holds the
+//   first halves of pairs [32 j, 32 j + np), box 1 at channel xb their second
+//   halves; its outputs are stored directly, pair by pair. Pair block 0 also
+//   owns the nope channels [nope & ~7, nope), the first columns of its box 0.
 struct Tile {
   int rt, ct, row0, c0, nch;
   int64_t s0;
   bool has_pe;
+  int kind, xa, xb, j, np;
 };
+
+// channel of the first column of box k of a tile
+__device__ __forceinline__ int box_x(const Tile& x, int k) { return k == 0 ? x.xa : x.xb; }
 
 // Tile (rt, ct): row tile rt, channel tile ct.
 template <bool BWD, bool WIDE = false>
@@ -169,11 +191,31 @@ __device__ __forceinline__ Tile make_tile(const PostmixParams& p, int rt, int ct
   x.rt = rt;
   x.ct = ct;
   x.row0 = x.rt * p.R;
-  x.c0 = x.ct * C::NC;
-  const int left = p.d - x.c0;
-  x.nch = min(C::kChunks, (left + kChunkCols - 1) / kChunkCols);
   x.s0 = static_cast<int64_t>(x.rt) * p.P;
-  x.has_pe = (p.nope / C::NC) == x.ct;
+  x.j = 0;
+  x.np = 0;
+  // the general tiling occurs in the forward and the 128-channel backward only
+  constexpr bool kGen = !BWD || WIDE;
+  const bool gen = kGen && p.gen;
+  if (!gen || ct < p.n_nope_ct) {
+    x.c0 = x.ct * C::NC;
+    const int left = (gen ? (p.nope & ~7) : p.d) - x.c0;
+    x.nch = min(C::kChunks, (left + kChunkCols - 1) / kChunkCols);
+    x.has_pe = !gen && (p.nope / C::NC) == x.ct;
+    x.kind = gen ? 1 : 0;
+    x.xa = x.c0;
+    x.xb = x.c0 + kChunkCols;
+  } else {
+    const int half = p.pe >> 1;
+    x.j = ct - p.n_nope_ct;
+    x.np = min(32, half - 32 * x.j);
+    x.xa = (p.nope + 32 * x.j) & ~7;
+    x.xb = (p.nope + half + 32 * x.j) & ~7;
+    x.c0 = x.xa;
+    x.nch = 2;
+    x.has_pe = true;
+    x.kind = 2;
+  }
   return x;
 }
 
@@ -212,6 +254,16 @@ __device__ __forceinline__ bool wait_bar_for(uint32_t bar, uint32_t parity, vola
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          unsigned code) {
   return wait_bar_for(bar, parity, abort_flag, code, kWaitLimitNs);
+}
+
+// Bounded wait that ignores the abort flag: for completions that must land
+// before the CTA frees what they write to (in-flight MMAs, a bulk copy).
+__device__ __forceinline__ bool wait_bar_noabort(uint32_t bar, uint32_t parity) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity))
+    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  return true;
 }
 
 // One thread waits for phase 0 of an mbarrier that nothing ever arrives on:
@@ -261,6 +313,34 @@ __device__ __forceinline__ void fill_rot_table(float2* tab, const uint64_t* F, c
     const uint64_t turns = static_cast<uint64_t>(p.pos0 + rel) * F[i];
     const int32_t ti = static_cast<int32_t>(turns >> 32);
     const float tf = static_cast<float>(ti) * 2.3283064365386963e-10f;  // turns, 2^-32 units
+    float sn, cs;
+    __sincosf(6.28318530717958648f * tf, &sn, &cs);
+    tab[k] = make_float2(cs, sn);
+  }
+}
+
+// Rotary frequency of pair i as turns per position in 0.64 fixed point, formed
+// on the device (pairs beyond the first 32, whose values the host does not pass).
+__device__ __forceinline__ uint64_t freq_turns_fixed(int i, int pe, double log2_theta) {
+  const double f = exp2(-2.0 * static_cast<double>(i) / static_cast<double>(pe) * log2_theta);
+  return static_cast<uint64_t>(llrint(ldexp(f * 0.15915494309189535, 63))) << 1;
+}
+
+// The general tiling's pair block j: cos/sin of pairs 32 j + ii (ii < np) for
+// the P positions of the tile starting at row s0, entry pl * 32 + ii.
+__device__ __forceinline__ void fill_rot_table_gen(float2* tab, const uint64_t* F, const PostmixParams& p,
+                                                   int64_t s0, int j, int np, int tid, int nthr) {
+  const int n = p.P * 32;
+  for (int k = tid; k < n; k += nthr) {
+    const int pl = k >> 5, ii = k & 31;
+    if (ii >= np) continue;
+    const int i = 32 * j + ii;
+    const uint64_t Fi = i < kMaxHalf ? F[i] : freq_turns_fixed(i, p.pe, p.log2_theta);
+    const int64_t s = s0 + pl;
+    const int64_t rel = p.pos ? (s < p.sq ? static_cast<int64_t>(__ldg(p.pos + s)) : 0) : s;
+    const uint64_t turns = static_cast<uint64_t>(p.pos0 + rel) * Fi;
+    const int32_t ti = static_cast<int32_t>(turns >> 32);
+    const float tf = static_cast<float>(ti) * 2.3283064365386963e-10f;
     float sn, cs;
     __sincosf(6.28318530717958648f * tf, &sn, &cs);
     tab[k] = make_float2(cs, sn);
@@ -317,6 +397,8 @@ template <bool BWD, bool WIDE = false>
 __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
     postmix_kernel(const __grid_constant__ PostmixParams p) {
   using C = KCfg<BWD, WIDE>;
+  // the general tiling's pair blocks occur in the forward and the 128-channel backward only
+  constexpr bool kGen = !BWD || WIDE;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -368,6 +450,10 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
   auto acc_phase = [&](uint32_t i) { return BWD ? (i >> na_sh) & 1u : (i / NA) & 1u; };
 
   // ------------------------------------------------------------ setup
+  // thread 0 (the TMA producer) issues the slot acquisition first; its result
+  // is needed only at the end of the barrier set-up
+  bool sched_mine = false;
+  if (!BWD && threadIdx.x == 0) sched_mine = sched_acquire(p.sched, launch_tag());
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(bar_full(s), 1);
@@ -388,6 +474,9 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
     ptx::mbar_init(bar_x_go, 1);
     ptx::mbar_init(bar_m, 1);
     *abort_flag = 0;
+    // forward: take the launch's counter slot; if another launch still holds
+    // it, claim nothing from it and wind down (outputs undefined, fault recorded)
+    if (!BWD && !sched_mine) record_fault(INVROPE_FAULT_SCHED_BUSY_FWD, abort_flag);
     ptx::fence_mbar_init();
     // forward: M goes out first, ahead of every tile load; the A build waits on it
     if (!BWD && p.m_bulk) {
@@ -412,7 +501,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
       for (int o = lane * 128; o < mbytes; o += 32 * 128) ptx::prefetch_l2(mb + o);
     __syncwarp();
   }
-  if (threadIdx.x < half) F[threadIdx.x] = p.F[threadIdx.x];
+  if (threadIdx.x < half && threadIdx.x < kMaxHalf) F[threadIdx.x] = p.F[threadIdx.x];
   // Rows >= R of every 64-channel box are never loaded and must read as 0
   // (the MMA's K range covers them).
   if (p.R < kRowsMax) {
@@ -538,6 +627,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
         const int st = static_cast<int>(i % S);
         const uint32_t ph = (i / S) & 1u;
         if (BWD && t_next >= t_end) break;
+        if (*abort_flag) break;
         if (!wait_bar(bar_empty(st), ph ^ 1u, abort_flag, (kRoleProducer << 8) | kBarEmpty)) break;
         const int64_t t = t_next;
         if (BWD) {
@@ -548,22 +638,25 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
             ptx::mbar_arrive(bar_full(st));
             break;
           }
-          t_next = static_cast<int64_t>(gridDim.x) + static_cast<int64_t>(atomicAdd(p.sched, 1u));
+          t_next = static_cast<int64_t>(gridDim.x) + static_cast<int64_t>(atomicAdd(&p.sched->next, 1u));
           stage_tile[st] = static_cast<int>(t);
         }
         const Tile x = decode_tile<BWD, WIDE>(p, t);
-        INVROPE_DBG_CHECK(t >= 0 && t < p.n_tiles && x.row0 >= 0 && x.c0 % kChunkCols == 0 && x.c0 < p.d &&
-                              x.nch >= 1 && x.nch <= C::kChunks,
+        INVROPE_DBG_CHECK(t >= 0 && t < p.n_tiles && x.row0 >= 0 && x.xa % 8 == 0 && x.xa < p.d &&
+                              (x.nch < 2 || (x.xb % 8 == 0 && x.xb < p.d)) && x.nch >= 1 && x.nch <= C::kChunks,
                           2);
         const uint32_t bytes = static_cast<uint32_t>(x.nch * p.R * 128 * (BWD ? 2 : 1));
         ptx::mbar_arrive_expect_tx(bar_full(st), bytes);
         const uint32_t sa = stage_addr(st);
-        for (int k = 0; k < x.nch; ++k)
-          ptx::tma_load_2d(sa + k * kChunkBytes, &p.tm_in0, x.c0 + k * kChunkCols, x.row0, bar_full(st));
-        if (BWD)
+        // general pe tiles read all d channels; every other tile reads through
+        // tm_in0 / tm_in1 (clipped at channel nope under the general tiling)
+        const CUtensorMap* m0 = (kGen && x.kind == 2) ? &p.tm_in0_pe : &p.tm_in0;
+        for (int k = 0; k < x.nch; ++k) ptx::tma_load_2d(sa + k * kChunkBytes, m0, box_x(x, k), x.row0, bar_full(st));
+        if (BWD) {
+          const CUtensorMap* m1 = (kGen && x.kind == 2) ? &p.tm_in1_pe : &p.tm_in1;
           for (int k = 0; k < x.nch; ++k)
-            ptx::tma_load_2d(sa + C::kTensorTile + k * kChunkBytes, &p.tm_in1, x.c0 + k * kChunkCols,
-                             x.row0, bar_full(st));
+            ptx::tma_load_2d(sa + C::kTensorTile + k * kChunkBytes, m1, box_x(x, k), x.row0, bar_full(st));
+        }
       }
     }
     __syncwarp();  // the whole warp reaches the teardown barrier together
@@ -587,12 +680,17 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
             d2_started = 1;
           }
         if (x.has_pe) {
-          const int kpe = (p.nope - x.c0) / kChunkCols;
-          for (uint32_t kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = ptx::smem_desc_sw128(sa + kpe * kChunkBytes + kk * 32, 16, 1024);
-            const uint64_t bd = ptx::smem_desc_sw128(base + C::kOffXlo + kk * 32, 16, 1024);
-            ptx::tc_mma_ss(d2, ad, bd, idesc_dm, 1);
-          }
+          // the lo terms of X: one box (the pe box of a regular tile) or both
+          // boxes of a general pair block, X_lo box b pairing with dY box kpe + b
+          const bool gen_pe = kGen && x.kind == 2;
+          const int kpe = gen_pe ? 0 : (p.nope - x.c0) / kChunkCols;
+          const int nlo = gen_pe ? 2 : 1;
+          for (int b = 0; b < nlo; ++b)
+            for (uint32_t kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = ptx::smem_desc_sw128(sa + (kpe + b) * kChunkBytes + kk * 32, 16, 1024);
+              const uint64_t bd = ptx::smem_desc_sw128(base + C::kOffXlo + b * kChunkBytes + kk * 32, 16, 1024);
+              ptx::tc_mma_ss(d2, ad, bd, idesc_dm, 1);
+            }
         }
       };
       // the pe tile whose dM chain is still to be issued (stage, tile)
@@ -680,8 +778,9 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
       }
       if (BWD && pend_st >= 0) flush_pending();
       if (BWD) ptx::tc_commit(bar_d2);
+      // every MMA issued must complete before TMEM is freed, abort or not
       ptx::tc_commit(bar_done);
-      wait_bar(bar_done, 0, abort_flag, (kRoleMma << 8) | kBarDone);
+      wait_bar_noabort(bar_done, 0);
     }
     __syncwarp();
   } else if (warp < 6) {
@@ -740,6 +839,72 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
       if (BWD && ++e_ct == p.n_ct) {
         e_ct = 0;
         ++e_rt;
+      }
+      if (kGen && x.kind == 2) {
+        // General pair block: accumulator columns [0, 64) are box 0, [64, 128)
+        // box 1; pair ii has its first half at column da + ii and its second
+        // half at column db + ii. Rotate, round once, store both halves
+        // straight to global memory (the boxes also hold channels of other
+        // pairs, so they are not stored whole).
+        fill_rot_table_gen(tab, F, p, x.s0, x.j, x.np, e, 128);
+        ptx::named_bar_sync(1, 128);
+        const uint32_t ta = tmem_base + lane_addr + static_cast<uint32_t>(acc) * acc_cols;
+        const int c1 = p.nope + 32 * x.j, c2 = c1 + half;
+        const int da = c1 - x.xa, db = kChunkCols + c2 - x.xb;
+        const int64_t grow = static_cast<int64_t>(x.row0) + r;
+        const bool live = row_ok && grow < p.rows;
+        uint16_t* yrow = p.out + grow * p.d;
+        const float2* rt = tab + pl * 32;
+        if (x.j == 0)  // nope channels [xa, nope): plain head mix, rounded once
+          for (int ii = 0; ii < da; ++ii) {
+            uint32_t a;
+            ptx::tmem_ld_x1(ta + ii, a);
+            ptx::tmem_ld_wait(a);
+            if (live) yrow[x.xa + ii] = bf16_bits(__uint_as_float(a));
+          }
+        if (da == 0 && db == kChunkCols && (x.np & 7) == 0) {
+          for (int i0 = 0; i0 < x.np; i0 += 8) {
+            uint32_t a[8], bb[8];
+            ptx::tmem_ld_x8(ta + i0, a);
+            ptx::tmem_ld_x8(ta + kChunkCols + i0, bb);
+            ptx::tmem_ld_wait(a, bb);
+            if (live) {
+              uint32_t w1[4], w2[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                float y1[2], y2[2];
+#pragma unroll
+                for (int s2 = 0; s2 < 2; ++s2) {
+                  const int kq = 2 * q + s2;
+                  const float2 cs = rt[i0 + kq];
+                  const float x1 = __uint_as_float(a[kq]), x2 = __uint_as_float(bb[kq]);
+                  y1[s2] = x1 * cs.x - sgn * x2 * cs.y;
+                  y2[s2] = x2 * cs.x + sgn * x1 * cs.y;
+                }
+                w1[q] = ptx::pack_bf16x2(y1[0], y1[1]);
+                w2[q] = ptx::pack_bf16x2(y2[0], y2[1]);
+              }
+              *reinterpret_cast<uint4*>(yrow + c1 + i0) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+              *reinterpret_cast<uint4*>(yrow + c2 + i0) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+            }
+          }
+        } else {
+          for (int ii = 0; ii < x.np; ++ii) {
+            uint32_t a, bb;
+            ptx::tmem_ld_x1(ta + da + ii, a);
+            ptx::tmem_ld_x1(ta + db + ii, bb);
+            ptx::tmem_ld_wait(a, bb);
+            if (live) {
+              const float2 cs = rt[ii];
+              const float x1 = __uint_as_float(a), x2 = __uint_as_float(bb);
+              yrow[c1 + ii] = bf16_bits(x1 * cs.x - sgn * x2 * cs.y);
+              yrow[c2 + ii] = bf16_bits(x2 * cs.x + sgn * x1 * cs.y);
+            }
+          }
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_acc_empty(acc));
+        continue;
       }
       const int pcol = p.nope - x.c0;  // tile-relative column of the first pe channel
       if (x.has_pe) {
@@ -1008,7 +1173,13 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
       for (uint32_t i = 0; ok; ++i) {
         if (BWD && t_begin + i >= t_end) break;
         const int64_t tb = t_begin + i;
-        const int nk = BWD ? decode_tile<BWD, WIDE>(p, tb).nch : 1;  // forward: one chunk per hand-off
+        // forward: one chunk per hand-off; backward: every box of a tile, none
+        // of a general pair block (stored directly by the epilogue)
+        int nk = 1;
+        if (BWD) {
+          const Tile xb = decode_tile<BWD, WIDE>(p, tb);
+          nk = (kGen && xb.kind == 2) ? 0 : xb.nch;
+        }
         for (int kk = 0; kk < nk; ++kk, ++n) {
           const int b = static_cast<int>(n % OB);
           if (!wait_bar(bar_ob_full(b), (n / OB) & 1u, abort_flag,
@@ -1023,8 +1194,8 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
           }
           const int k = BWD ? kk : ob_chunk[b];
           const Tile x = decode_tile<BWD, WIDE>(p, t);
-          INVROPE_DBG_CHECK(b < OB && k < x.nch && x.c0 + k * kChunkCols < p.d, 6);
-          ptx::tma_store_2d(&p.tm_out, out_addr(b), x.c0 + k * kChunkCols, x.row0);
+          INVROPE_DBG_CHECK(b < OB && k < x.nch && x.kind != 2 && box_x(x, k) < p.d, 6);
+          ptx::tma_store_2d(&p.tm_out, out_addr(b), box_x(x, k), x.row0);
           ptx::bulk_commit();
           // keep kIn stores reading; recycle the buffer of the oldest finished one
           if (n + 1u >= static_cast<uint32_t>(kIn)) {
@@ -1059,6 +1230,84 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
         if (!group_wait(bar_x_empty, static_cast<uint32_t>((npe & 1) ^ 1), abort_flag,
                         (kRoleTransform << 8) | kBarXEmpty, xr == 0, slot_xf_empty, 2))
           break;
+        if (kGen && x.kind == 2) {
+          // General pair block: X = invrope(O) for its pairs (first halves in
+          // O box 0 at column da + ii, second halves in box 1 at db + ii), hi
+          // in place, lo into X_lo; every other column of both boxes is set to
+          // 0 in both, so that dM counts each channel once (in its own tile).
+          fill_rot_table_gen(tab, F, p, x.s0, x.j, x.np, xr, 128);
+          ptx::named_bar_sync(2, 128);
+          if (xr < p.R) {
+            const uint32_t oc = stage_addr(st) + C::kTensorTile;
+            const uint32_t xl = base + C::kOffXlo;
+            const int c1 = p.nope + 32 * x.j, c2 = c1 + half;
+            const int da = c1 - x.xa, db = kChunkCols + c2 - x.xb;
+            const int np = x.np;
+            const float2* rt = tab + (xr / p.nh) * 32;
+            if (da == 0 && db == kChunkCols && (np & 7) == 0) {
+              for (int i0 = 0; i0 < np; i0 += 8) {
+                const uint32_t a1 = swz_unit_addr(oc, xr, i0);
+                const uint32_t a2 = swz_unit_addr(oc, xr, kChunkCols + i0);
+                uint32_t u1[4], u2[4];
+                ptx::ld_shared_v4(a1, u1[0], u1[1], u1[2], u1[3]);
+                ptx::ld_shared_v4(a2, u2[0], u2[1], u2[2], u2[3]);
+                uint32_t h1[4], h2[4], l1[4], l2[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  float X1[2], X2[2];
+#pragma unroll
+                  for (int s2 = 0; s2 < 2; ++s2) {
+                    const float2 cs = rt[i0 + 2 * q + s2];
+                    const float x1 = s2 ? ptx::bf16_hi_f32(u1[q]) : ptx::bf16_lo_f32(u1[q]);
+                    const float x2 = s2 ? ptx::bf16_hi_f32(u2[q]) : ptx::bf16_lo_f32(u2[q]);
+                    X1[s2] = x1 * cs.x + x2 * cs.y;
+                    X2[s2] = x2 * cs.x - x1 * cs.y;
+                  }
+                  h1[q] = ptx::pack_bf16x2(X1[0], X1[1]);
+                  h2[q] = ptx::pack_bf16x2(X2[0], X2[1]);
+                  l1[q] = ptx::pack_bf16x2(X1[0] - ptx::bf16_lo_f32(h1[q]), X1[1] - ptx::bf16_hi_f32(h1[q]));
+                  l2[q] = ptx::pack_bf16x2(X2[0] - ptx::bf16_lo_f32(h2[q]), X2[1] - ptx::bf16_hi_f32(h2[q]));
+                }
+                ptx::st_shared_v4(a1, h1[0], h1[1], h1[2], h1[3]);
+                ptx::st_shared_v4(a2, h2[0], h2[1], h2[2], h2[3]);
+                ptx::st_shared_v4(swz_unit_addr(xl, xr, i0), l1[0], l1[1], l1[2], l1[3]);
+                ptx::st_shared_v4(swz_unit_addr(xl, xr, kChunkCols + i0), l2[0], l2[1], l2[2], l2[3]);
+              }
+              for (int u = np >> 3; u < 8; ++u)
+                for (int bx = 0; bx < 2; ++bx) {
+                  ptx::st_shared_v4(swz_unit_addr(oc, xr, bx * kChunkCols + 8 * u), 0u, 0u, 0u, 0u);
+                  ptx::st_shared_v4(swz_unit_addr(xl, xr, bx * kChunkCols + 8 * u), 0u, 0u, 0u, 0u);
+                }
+            } else {
+              for (int ii = 0; ii < np; ++ii) {
+                const int k1 = da + ii, k2 = db + ii;
+                const uint32_t a1 = swz_unit_addr(oc, xr, k1) + (k1 & 7) * 2;
+                const uint32_t a2 = swz_unit_addr(oc, xr, k2) + (k2 & 7) * 2;
+                const float x1 = bf16_bits_to_f32(ld_shared_b16(a1));
+                const float x2 = bf16_bits_to_f32(ld_shared_b16(a2));
+                const float2 cs = rt[ii];
+                const float X1 = x1 * cs.x + x2 * cs.y, X2 = x2 * cs.x - x1 * cs.y;
+                const uint16_t hb1 = bf16_bits(X1), hb2 = bf16_bits(X2);
+                st_shared_b16(a1, hb1);
+                st_shared_b16(a2, hb2);
+                st_shared_b16(swz_unit_addr(xl, xr, k1) + (k1 & 7) * 2, bf16_bits(X1 - bf16_bits_to_f32(hb1)));
+                st_shared_b16(swz_unit_addr(xl, xr, k2) + (k2 & 7) * 2, bf16_bits(X2 - bf16_bits_to_f32(hb2)));
+              }
+              // pair block 0 owns the nope channels [xa, nope) in columns
+              // [0, da): X = O there (hi as loaded, lo 0)
+              const int own0 = x.j == 0 ? da : 0;
+              for (int k = 0; k < 2 * kChunkCols; ++k) {
+                if ((k >= da && k < da + np) || (k >= db && k < db + np)) continue;
+                if (k >= own0) st_shared_b16(swz_unit_addr(oc, xr, k) + (k & 7) * 2, 0);
+                st_shared_b16(swz_unit_addr(xl, xr, k) + (k & 7) * 2, 0);
+              }
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          ptx::mbar_arrive(bar_x_full);
+          ++npe;
+          continue;
+        }
         fill_rot_table(tab, F, p, x.s0, half, xr, 128);
         ptx::named_bar_sync(2, 128);
         if (xr < p.R) {
@@ -1125,11 +1374,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
   // M's bulk copy must have landed before the CTA leaves (it has, unless the
   // CTA gave up early): bounded wait that ignores the abort flag
   if constexpr (!BWD) {
-    if (p.m_bulk && threadIdx.x == 0 && !ptx::mbar_try_wait(bar_m, 0)) {
-      const uint64_t t0 = ptx::globaltimer_ns();
-      while (!ptx::mbar_try_wait(bar_m, 0) && ptx::globaltimer_ns() - t0 < kWaitLimitNs) {
-      }
-    }
+    if (p.m_bulk && threadIdx.x == 0) wait_bar_noabort(bar_m, 0);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -1137,42 +1382,50 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::kTmemCols);
   }
-  if (!BWD && threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
-      p.sched[0] = 0u;
-      p.sched[1] = 0u;
-      __threadfence();
-    }
-  }
+  if (!BWD && threadIdx.x == 0 && sched_mine) sched_release(p.sched, gridDim.x);
 }
 
-// dM[o] = sum over the CTA partials ws[c][src(o)] in a fixed order: thread row
-// ty sums c = ty, ty+8, ... in fp64, then row 0 adds the 8 row sums in order.
-// The partials are [nh, nh]; a grouped mix keeps only its diagonal blocks:
-// output o = (k, i, j) of [nh/gs, gs, gs] reads entry (k gs + i, k gs + j).
-constexpr int kReduceRows = 8;
+// dM[o] = sum of the CTA partials ws[c][src(o)] (each [nh, nh]) in a fixed
+// order. A thread block takes 32 outputs (one per lane); warp w sums partials
+// c = w, w + 32, ... in fp32 with a compensation term (Kahan), and warp 0
+// then adds the 32 warp sums in order. fp64 arithmetic is scarce on this GPU,
+// so the per-element adds stay in fp32; the compensated sum keeps the error
+// near one fp32 rounding of the total. A grouped mix keeps only the diagonal
+// blocks: output o = (k, i, j) of [nh/gs, gs, gs] reads entry (k gs + i, k gs + j).
+constexpr int kReduceWarps = 32;
 
-__global__ void __launch_bounds__(32 * kReduceRows)
+__global__ void __launch_bounds__(32 * kReduceWarps)
     dm_reduce_kernel(const float* __restrict__ ws, float* __restrict__ dM, int nparts, int nh, int gs) {
-  __shared__ double part[kReduceRows][32];
+  __shared__ float part_s[kReduceWarps][33];
+  __shared__ float part_c[kReduceWarps][33];
   ptx::griddep_wait();  // launched early (programmatic dependent launch): wait for the partials
   const int nn = nh * nh, n_out = nh * gs;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int idx = blockIdx.x * 32 + tx;
   const int k = idx / (gs * gs), rem = idx - k * gs * gs;
   const int src = (k * gs + rem / gs) * nh + k * gs + rem % gs;
-  double s = 0.0;
+  float sum = 0.f, comp = 0.f;
   if (idx < n_out) {
-#pragma unroll 4
-    for (int c = ty; c < nparts; c += kReduceRows) s += static_cast<double>(ws[static_cast<int64_t>(c) * nn + src]);
+#pragma unroll 8
+    for (int c = ty; c < nparts; c += kReduceWarps) {
+      const float y = __ldg(ws + static_cast<int64_t>(c) * nn + src) - comp;
+      const float t = sum + y;
+      comp = (t - sum) - y;
+      sum = t;
+    }
   }
-  part[ty][tx] = s;
+  part_s[ty][tx] = sum;
+  part_c[ty][tx] = comp;
   __syncthreads();
   if (ty == 0 && idx < n_out) {
-    double t = 0.0;
-    for (int k = 0; k < kReduceRows; ++k) t += part[k][tx];
-    dM[idx] = static_cast<float>(t);
+    float s2 = 0.f, c2 = 0.f;
+    for (int w = 0; w < kReduceWarps; ++w) {
+      const float y = part_s[w][tx] - (part_c[w][tx] + c2);
+      const float t = s2 + y;
+      c2 = (t - s2) - y;
+      s2 = t;
+    }
+    dM[idx] = s2;
   }
 }
 
@@ -1191,11 +1444,57 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-// 2-D bf16 view [rows, d] with 64 x box_rows boxes, 128-byte swizzle.
-bool make_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int d, int box_rows) {
+// Encoded tensor maps of recent calls: a map depends only on the pointer and
+// the view's geometry, so a caller that reuses its buffers (every layer of a
+// model does) skips the encoding. Small, round-robin, one lock.
+struct TmapKey {
+  const void* ptr;
+  int64_t rows;
+  int d, width, box_rows;
+  bool operator==(const TmapKey& o) const {
+    return ptr == o.ptr && rows == o.rows && d == o.d && width == o.width && box_rows == o.box_rows;
+  }
+};
+struct TmapCache {
+  static constexpr int kEntries = 32;
+  std::mutex mu;
+  TmapKey key[kEntries] = {};
+  CUtensorMap map[kEntries];
+  bool used[kEntries] = {};
+  int next = 0;
+};
+TmapCache g_tmap_cache;
+
+bool encode_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int d, int width, int box_rows);
+
+// 2-D bf16 view [rows, d] (row stride d) with 64 x box_rows boxes, 128-byte
+// swizzle. Channels at or beyond `width` (<= d) lie outside the view: loads
+// read them as zero and stores leave them alone.
+bool make_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int d, int width, int box_rows) {
+  const TmapKey k{ptr, rows, d, width, box_rows};
+  TmapCache& c = g_tmap_cache;
+  {
+    std::lock_guard<std::mutex> lock(c.mu);
+    for (int i = 0; i < TmapCache::kEntries; ++i)
+      if (c.used[i] && c.key[i] == k) {
+        *m = c.map[i];
+        return true;
+      }
+  }
+  if (!encode_tmap(m, ptr, rows, d, width, box_rows)) return false;
+  std::lock_guard<std::mutex> lock(c.mu);
+  const int i = c.next;
+  c.next = (c.next + 1) % TmapCache::kEntries;
+  c.key[i] = k;
+  c.map[i] = *m;
+  c.used[i] = true;
+  return true;
+}
+
+bool encode_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int d, int width, int box_rows) {
   auto fn = get_encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(kChunkCols), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
@@ -1206,31 +1505,76 @@ bool make_tmap(CUtensorMap* m, const void* ptr, int64_t rows, int d, int box_row
 
 // Rotary frequency f_i = theta^(-2i/pe) as turns per position in 0.64 fixed
 // point: the kernel reduces pos * F[i] mod 2^64 exactly to a fractional turn.
+// The last (pe, theta) table of each host thread is kept.
 void fill_freq(uint64_t* F, int pe, double theta) {
-  for (int i = 0; i < pe / 2 && i < kMaxHalf; ++i) {
-    const double f = std::pow(theta, -2.0 * i / pe);
-    F[i] = static_cast<uint64_t>(std::llround(std::ldexp(f * 0.15915494309189535, 63))) << 1;
+  thread_local int last_pe = 0;
+  thread_local double last_theta = 0.0;
+  thread_local uint64_t last_F[kMaxHalf];
+  const int n = pe / 2 < kMaxHalf ? pe / 2 : kMaxHalf;
+  if (pe != last_pe || theta != last_theta) {
+    for (int i = 0; i < n; ++i) {
+      const double f = std::pow(theta, -2.0 * i / pe);
+      last_F[i] = static_cast<uint64_t>(std::llround(std::ldexp(f * 0.15915494309189535, 63))) << 1;
+    }
+    last_pe = pe;
+    last_theta = theta;
   }
+  std::memcpy(F, last_F, sizeof(uint64_t) * n);
 }
 
 struct Shape {
-  int P, R, n_ct;
+  int P, R, n_ct, n_nope_ct;
   int64_t n_tiles;
+  bool gen;   // general tiling: the pe block does not lie inside one 64-channel box
+  bool wide;  // backward: 128-channel tiles (one position per tile, or the general tiling)
 };
 
-int check_shape(int64_t sq, int nh, int nope, int pe, int nc, Shape* s) {
+// Validate a postmix shape and lay out its tiles (forward, or backward if bwd).
+int check_shape(int64_t sq, int nh, int nope, int pe, bool bwd, Shape* s) {
   if (sq < 0 || nh < 1 || nope < 0 || pe < 2 || (pe & 1)) return INVROPE_ERR_INVALID_ARG;
   const int64_t d = static_cast<int64_t>(nope) + pe;
   if (d % 8 != 0 || d > (1 << 20)) return INVROPE_ERR_INVALID_ARG;
   if (nh > 128) return INVROPE_ERR_UNSUPPORTED;
-  if (nope / kChunkCols != (d - 1) / kChunkCols) return INVROPE_ERR_UNSUPPORTED;
+  // rows of the [sq*nh, d] view are 32-bit TMA coordinates
   if (sq * nh >= (int64_t(1) << 31)) return INVROPE_ERR_UNSUPPORTED;
+  s->gen = nope / kChunkCols != (d - 1) / kChunkCols;
+  s->wide = bwd && (s->gen || nh > 64);
+  const int nc = (!bwd || s->wide) ? 2 * kChunkCols : kChunkCols;
   s->P = 128 / nh < kPosPerTileMax ? 128 / nh : kPosPerTileMax;
   s->R = s->P * nh;
-  s->n_ct = static_cast<int>((d + nc - 1) / nc);
+  if (!s->gen) {
+    s->n_nope_ct = 0;
+    s->n_ct = static_cast<int>((d + nc - 1) / nc);
+  } else {
+    s->n_nope_ct = ((nope & ~7) + nc - 1) / nc;
+    s->n_ct = s->n_nope_ct + (pe / 2 + 31) / 32;
+  }
   s->n_tiles = ((sq + s->P - 1) / s->P) * s->n_ct;
   if (s->n_tiles >= (int64_t(1) << 31)) return INVROPE_ERR_UNSUPPORTED;
   return INVROPE_OK;
+}
+
+// The tensor maps of a launch: in0 (and in1) read, out written. Under the
+// general tiling the maps of the nope tiles end at channel nope & ~7, and the
+// pair blocks read through the full-width *_pe maps.
+bool make_maps(PostmixParams* p, const Shape& s, const void* in0, const void* in1, void* out, int64_t rows,
+               int nope, int d) {
+  // (a clip must fall on a 16-byte boundary: channels [nope & ~7, nope) go
+  // with the first pair block)
+  const int width = (s.gen && (nope & ~7) > 0) ? (nope & ~7) : d;
+  if (!make_tmap(&p->tm_in0, in0, rows, d, width, s.R) || !make_tmap(&p->tm_out, out, rows, d, width, s.R))
+    return false;
+  if (in1 && !make_tmap(&p->tm_in1, in1, rows, d, width, s.R)) return false;
+  if (!in1) p->tm_in1 = p->tm_in0;
+  if (!s.gen) {
+    p->tm_in0_pe = p->tm_in0;
+    p->tm_in1_pe = p->tm_in1;
+    return true;
+  }
+  if (!make_tmap(&p->tm_in0_pe, in0, rows, d, d, s.R)) return false;
+  if (in1 && !make_tmap(&p->tm_in1_pe, in1, rows, d, d, s.R)) return false;
+  if (!in1) p->tm_in1_pe = p->tm_in0_pe;
+  return true;
 }
 
 template <bool BWD, bool WIDE = false>
@@ -1251,32 +1595,22 @@ int ensure_smem_attr(int device) {
 
 bool valid_theta(double theta) { return std::isfinite(theta) && theta > 0.0; }
 
-// This launch's schedule counters on the current device: the address of
-// g_sched is looked up once per device; slots rotate per launch.
-int sched_slot(int device, unsigned int** out) {
-  static std::mutex mu;
-  static unsigned int* base[64] = {};
-  static unsigned int seq[64] = {};
-  if (device < 0 || device >= 64) return INVROPE_ERR_DEVICE;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!base[device]) {
-    void* ptr = nullptr;
-    const cudaError_t err = cudaGetSymbolAddress(&ptr, g_sched);
-    if (err != cudaSuccess) return cuda_fail(err);
-    base[device] = static_cast<unsigned int*>(ptr);
-  }
-  *out = base[device] + 2 * (seq[device]++ % kSchedSlots);
-  return INVROPE_OK;
-}
+SlotRing g_sched_ring;
 
 }  // namespace
 
+int reset_postmix_sched(int device) { return slot_reset_all(g_sched_ring, &g_sched, device); }
+
+int occupy_postmix_slot(int device, unsigned long long owner) {
+  SchedSlot* s = nullptr;
+  const int st = slot_peek_eager(g_sched_ring, &g_sched, device, &s);
+  if (st != INVROPE_OK) return st;
+  const cudaError_t err = cudaMemcpy(&s->owner, &owner, sizeof(owner), cudaMemcpyHostToDevice);
+  return err == cudaSuccess ? INVROPE_OK : cuda_fail(err);
+}
+
 // Grid size of the backward kernel (one dM partial per CTA).
 static int64_t bwd_grid(const Shape& s, int sms) { return s.n_tiles < sms ? s.n_tiles : sms; }
-
-// The backward runs 128-channel tiles when a tile holds one position (nh > 64).
-static bool bwd_wide(int nh) { return nh > 64; }
-static int bwd_nc(int nh) { return bwd_wide(nh) ? KCfg<true, true>::NC : KCfg<true>::NC; }
 
 }  // namespace invrope
 
@@ -1295,7 +1629,7 @@ extern "C" int invrope_postmix_fwd_ex(const void* O, const float* M, void* Y, in
                                       int nope, int pe, const int32_t* positions, int64_t pos0, double theta,
                                       struct CUstream_st* stream) {
   Shape s;
-  int st = check_shape(sq, nh, nope, pe, KCfg<false>::NC, &s);
+  int st = check_shape(sq, nh, nope, pe, false, &s);
   if (st != INVROPE_OK) return st;
   if ((st = check_mix_args(nh, gs, positions, pos0, theta)) != INVROPE_OK) return st;
   if (sq == 0) return INVROPE_OK;
@@ -1311,12 +1645,13 @@ extern "C" int invrope_postmix_fwd_ex(const void* O, const float* M, void* Y, in
   PostmixParams p;
   std::memset(&p, 0, sizeof(p));
   const int d = nope + pe;
-  if (!make_tmap(&p.tm_in0, O, sq * nh, d, s.R) || !make_tmap(&p.tm_out, Y, sq * nh, d, s.R))
-    return INVROPE_ERR_CUDA;
-  p.tm_in1 = p.tm_in0;
+  if (!make_maps(&p, s, O, nullptr, Y, sq * nh, nope, d)) return INVROPE_ERR_CUDA;
+  p.out = static_cast<uint16_t*>(Y);
   p.M = M;
   p.ws = nullptr;
-  if ((st = sched_slot(dev.device, &p.sched)) != INVROPE_OK) return st;
+  if ((st = slot_take(g_sched_ring, &g_sched, dev.device, reinterpret_cast<cudaStream_t>(stream), &p.sched)) !=
+      INVROPE_OK)
+    return st;
   p.sq = sq;
   p.pos0 = pos0;
   p.n_tiles = s.n_tiles;
@@ -1330,6 +1665,10 @@ extern "C" int invrope_postmix_fwd_ex(const void* O, const float* M, void* Y, in
   p.n_ct = s.n_ct;
   p.pos = positions;
   p.gs = gs;
+  p.gen = s.gen ? 1 : 0;
+  p.n_nope_ct = s.n_nope_ct;
+  p.rows = sq * nh;
+  p.log2_theta = std::log2(theta);
   // M by one bulk copy at kernel start: 16-byte aligned, ungrouped, nh % 64 == 0
   p.m_bulk = (aligned(M, 16) && gs == nh && nh % 64 == 0) ? 1 : 0;
   fill_freq(p.F, pe, theta);
@@ -1346,7 +1685,7 @@ extern "C" int invrope_postmix_fwd(const void* O, const float* M, void* Y, int64
 
 extern "C" size_t invrope_postmix_bwd_workspace_bytes(int64_t sq, int nh, int nope, int pe) {
   Shape s;
-  if (check_shape(sq, nh, nope, pe, bwd_nc(nh), &s) != INVROPE_OK) return 0;
+  if (check_shape(sq, nh, nope, pe, true, &s) != INVROPE_OK) return 0;
   DeviceInfo dev;
   if (current_device(&dev) != INVROPE_OK) return 0;
   const int64_t grid = sq == 0 ? 1 : bwd_grid(s, dev.sms);
@@ -1358,7 +1697,7 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
                                       int nope, int pe, const int32_t* positions, int64_t pos0, double theta,
                                       struct CUstream_st* stream) {
   Shape s;
-  int st = check_shape(sq, nh, nope, pe, bwd_nc(nh), &s);
+  int st = check_shape(sq, nh, nope, pe, true, &s);
   if (st != INVROPE_OK) return st;
   if ((st = check_mix_args(nh, gs, positions, pos0, theta)) != INVROPE_OK) return st;
   if (!M || !dM || !aligned(M, 4) || !aligned(dM, 4)) return INVROPE_ERR_INVALID_ARG;
@@ -1384,15 +1723,14 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
   }
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (grid > 0) {
-    const bool wide = bwd_wide(nh);
+    const bool wide = s.wide;
     if ((st = wide ? ensure_smem_attr<true, true>(dev.device) : ensure_smem_attr<true>(dev.device)) != INVROPE_OK)
       return st;
     PostmixParams p;
     std::memset(&p, 0, sizeof(p));
     const int d = nope + pe;
-    if (!make_tmap(&p.tm_in0, dY, sq * nh, d, s.R) || !make_tmap(&p.tm_in1, O, sq * nh, d, s.R) ||
-        !make_tmap(&p.tm_out, dO, sq * nh, d, s.R))
-      return INVROPE_ERR_CUDA;
+    if (!make_maps(&p, s, dY, O, dO, sq * nh, nope, d)) return INVROPE_ERR_CUDA;
+    p.out = static_cast<uint16_t*>(dO);
     p.M = M;
     p.ws = static_cast<float*>(workspace);
     p.sq = sq;
@@ -1410,6 +1748,10 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
     p.stacked = (!wide && nh == 64 && pe == kChunkCols && nope % kChunkCols == 0) ? 1 : 0;
     p.pos = positions;
     p.gs = gs;
+    p.gen = s.gen ? 1 : 0;
+    p.n_nope_ct = s.n_nope_ct;
+    p.rows = sq * nh;
+    p.log2_theta = std::log2(theta);
     p.m_bulk = 0;  // the backward reads M from L2 (a bulk copy did not pay off there)
     fill_freq(p.F, pe, theta);
     if (wide)
@@ -1425,7 +1767,7 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
   // reduction blocks that start early crowd onto the first SMs to free up.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((nh * gs + 31) / 32));
-  cfg.blockDim = dim3(32 * kReduceRows);
+  cfg.blockDim = dim3(32 * kReduceWarps);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = cs;
   cudaLaunchAttribute attr[1];
@@ -1460,12 +1802,22 @@ extern "C" int invrope_watchdog_selftest(int64_t limit_us, int* fault) {
 
 extern "C" int invrope_take_device_fault(int* fault) {
   if (!fault) return INVROPE_ERR_INVALID_ARG;
-  cudaError_t err = cudaDeviceSynchronize();
+  int device = 0;
+  cudaError_t err = cudaGetDevice(&device);
   if (err != cudaSuccess) return cuda_fail(err);
-  unsigned v = 0;
+  if ((err = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(err);
+  unsigned v = 0, vr = 0;
   if ((err = cudaMemcpyFromSymbol(&v, g_fault_code, sizeof(v))) != cudaSuccess) return cuda_fail(err);
   const unsigned zero = 0;
   if ((err = cudaMemcpyToSymbol(g_fault_code, &zero, sizeof(zero))) != cudaSuccess) return cuda_fail(err);
+  int st = take_remap_fault(&vr);
+  if (st != INVROPE_OK) return st;
+  if (v == 0) v = vr;
+  // After a fault a launch may have left a work-counter slot held (its
+  // blocks that found the slot busy never release it): nothing runs on the
+  // device now, so every slot is returned to the free state.
+  if (v != 0 && ((st = reset_postmix_sched(device)) != INVROPE_OK || (st = reset_remap_sched(device)) != INVROPE_OK))
+    return st;
   *fault = static_cast<int>(v);
   return INVROPE_OK;
 }

@@ -267,6 +267,10 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&a)[8], uint32_t (&b)[8])
                : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld_wait(uint32_t& a) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(a) : : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait(uint32_t& a, uint32_t& b) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(a), "+r"(b) : : "memory");
 }

@@ -10,8 +10,9 @@
 // element range [b*sq*topk, (b+1)*sq*topk), so a thread block that walks a
 // chunk of the flat array finds its batch with one division per chunk and
 // at most one boundary inside it. 16-byte vectors when the layout allows.
-// Chunks are handed out dynamically (a per-launch counter): SMs differ in the
-// memory bandwidth they get, and a fixed split would wait on the slowest.
+// Chunks are handed out dynamically (a per-launch counter slot, sched.cuh):
+// SMs differ in the memory bandwidth they get, and a fixed split would wait on
+// the slowest.
 // int32 and int64 tables (the int64 one for callers that index past 2^31).
 #include <cuda_runtime.h>
 
@@ -19,14 +20,17 @@
 #include <mutex>
 
 #include "common.h"
+#include "sched.cuh"
 
 namespace invrope {
 
-// Dynamic chunk scheduling: one {next chunk, finished blocks} pair per launch
-// slot; a launch takes slot (launch sequence number mod kRemapSlots) and its
-// last block returns the pair to zero.
-constexpr int kRemapSlots = 256;
-__device__ unsigned long long g_remap_sched[kRemapSlots][2];
+// The remap's own fault word (each translation unit's device code is linked
+// separately): invrope_take_device_fault() reads and clears it together with
+// the postmix kernels' word.
+__device__ unsigned int g_remap_fault = 0;
+
+// Dynamic chunk scheduling: one work-counter slot per launch (sched.cuh).
+__device__ SchedSlot g_remap_sched[kSchedSlots];
 
 namespace {
 
@@ -71,12 +75,23 @@ __device__ __forceinline__ long long remap_vec(long long v, uint64_t off) { retu
 // kOneBoundary: seg >= kChunk, so a chunk crosses at most one batch boundary.
 template <typename V, bool kOneBoundary>
 __global__ void __launch_bounds__(kThreads) kv_remap_kernel(const V* in, V* out, int64_t n, int64_t seg,
-                                                            uint64_t seqlen_kv, unsigned long long* sched) {
+                                                            uint64_t seqlen_kv, SchedSlot* sched) {
   __shared__ int64_t next_chunk;
   const int64_t nchunks = (n + kChunk - 1) / kChunk;
+  // Thread 0 takes the launch's counter slot along with its first claim. A
+  // block that finds the slot held by another launch still in flight does its
+  // static first chunk, claims nothing and records a fault.
+  bool mine = false;
   // first chunk = block index; each later one is claimed while the current one streams
   for (int64_t ch = blockIdx.x; ch < nchunks;) {
-    if (threadIdx.x == 0) next_chunk = static_cast<int64_t>(gridDim.x + atomicAdd(sched, 1ull));
+    if (threadIdx.x == 0) {
+      if (ch == static_cast<int64_t>(blockIdx.x)) {
+        mine = sched_acquire(sched, launch_tag());
+        if (!mine) atomicCAS(&g_remap_fault, 0u, static_cast<unsigned>(INVROPE_FAULT_SCHED_BUSY_REMAP));
+      }
+      next_chunk = mine ? static_cast<int64_t>(gridDim.x) + static_cast<int64_t>(atomicAdd(&sched->next, 1u))
+                        : nchunks;
+    }
     const int64_t v0 = ch * kChunk;
     const int64_t b0 = v0 / seg;
     const int64_t boundary = (b0 + 1) * seg;
@@ -98,38 +113,16 @@ __global__ void __launch_bounds__(kThreads) kv_remap_kernel(const V* in, V* out,
     ch = next_chunk;
     __syncthreads();  // and read by all before thread 0 claims again
   }
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(sched + 1, 1ull) == gridDim.x - 1) {  // last block: reset the slot
-      sched[0] = 0;
-      sched[1] = 0;
-      __threadfence();
-    }
-  }
+  if (threadIdx.x == 0 && mine) sched_release(sched, gridDim.x);
 }
 
-// This launch's counter pair on device `device` (address looked up once per device).
-int remap_slot(int device, unsigned long long** out) {
-  static std::mutex mu;
-  static unsigned long long* base[64] = {};
-  static unsigned int seq[64] = {};
-  if (device < 0 || device >= 64) return INVROPE_ERR_DEVICE;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!base[device]) {
-    void* ptr = nullptr;
-    const cudaError_t err = cudaGetSymbolAddress(&ptr, g_remap_sched);
-    if (err != cudaSuccess) return cuda_fail(err);
-    base[device] = static_cast<unsigned long long*>(ptr);
-  }
-  *out = base[device] + 2 * (seq[device]++ % kRemapSlots);
-  return INVROPE_OK;
-}
+SlotRing g_remap_ring;
 
 template <typename V>
 int launch(const void* in, void* out, int64_t n, int64_t seg, uint64_t skv, const DeviceInfo& dev,
            cudaStream_t s) {
-  unsigned long long* sched = nullptr;
-  const int st = remap_slot(dev.device, &sched);
+  SchedSlot* sched = nullptr;
+  const int st = slot_take(g_remap_ring, &g_remap_sched, dev.device, s, &sched);
   if (st != INVROPE_OK) return st;
   const int64_t nchunks = (n + kChunk - 1) / kChunk;
   const int64_t slots = static_cast<int64_t>(dev.sms) * 8;
@@ -157,6 +150,25 @@ int check_remap(const void* idx, const void* out, int64_t rows, int topk, int64_
 }
 
 }  // namespace
+
+int take_remap_fault(unsigned int* code) {
+  cudaError_t err = cudaMemcpyFromSymbol(code, g_remap_fault, sizeof(*code));
+  if (err != cudaSuccess) return cuda_fail(err);
+  const unsigned int zero = 0;
+  if ((err = cudaMemcpyToSymbol(g_remap_fault, &zero, sizeof(zero))) != cudaSuccess) return cuda_fail(err);
+  return INVROPE_OK;
+}
+
+int reset_remap_sched(int device) { return slot_reset_all(g_remap_ring, &g_remap_sched, device); }
+
+int occupy_remap_slot(int device, unsigned long long owner) {
+  SchedSlot* s = nullptr;
+  const int st = slot_peek_eager(g_remap_ring, &g_remap_sched, device, &s);
+  if (st != INVROPE_OK) return st;
+  const cudaError_t err = cudaMemcpy(&s->owner, &owner, sizeof(owner), cudaMemcpyHostToDevice);
+  return err == cudaSuccess ? INVROPE_OK : cuda_fail(err);
+}
+
 }  // namespace invrope
 
 using namespace invrope;

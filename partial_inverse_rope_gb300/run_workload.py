@@ -9,7 +9,9 @@ Used to capture ncu profiles of one kernel on a case small enough to replay.
 With --time, each call is timed with CUDA events on its stream (after 3
 untimed repetitions; a 512 MiB buffer is rewritten between timed calls so that
 inputs smaller than the L2 are not served from it) and the median per call is
-printed with the algorithmic GB/s.
+printed with the algorithmic GB/s. With --host-cost N, each operation is
+enqueued N times back to back through the C ABI (arguments marshalled once,
+no synchronisation in between) and the host wall time per call is printed.
 """
 
 from __future__ import annotations
@@ -36,6 +38,8 @@ def main(argv=None):
     ap.add_argument("--config", choices=sorted(W.POSTMIX_CONFIGS), default=None,
                     help="take sq/nh/nope/pe/pos0 from a named config")
     ap.add_argument("--time", action="store_true", help="time each call (median over --reps)")
+    ap.add_argument("--host-cost", type=int, default=0, metavar="N",
+                    help="host wall time per call over N back-to-back enqueues")
     args = ap.parse_args(argv)
 
     ops = [o.strip() for o in args.ops.split(",") if o.strip()]
@@ -63,7 +67,9 @@ def main(argv=None):
         else:
             raise SystemExit(f"unknown op {op}")
 
-    if not args.time:
+    if args.host_cost:
+        host_cost(ops, c, O, dY, M, Y, dO, dM, ws, R, idx, out, args.host_cost)
+    elif not args.time:
         for _ in range(args.reps):
             for op in ops:
                 call(op)
@@ -89,6 +95,44 @@ def main(argv=None):
     fault = ir.invrope_take_device_fault()
     print(f"ran {args.reps} x {ops} at sq={c.sq} nh={c.nh} d={c.d}; watchdog fault code {fault}")
     return 1 if fault else 0
+
+
+def host_cost(ops, c, O, dY, M, Y, dO, dM, ws, R, idx, out, n):
+    """Host wall time per call of each op: the C-ABI entry point called n
+    times with pre-marshalled ctypes arguments, without synchronising."""
+    import ctypes
+    import time
+
+    lib = ir.lib()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    ws_bytes = ws.numel()
+    argsets = {
+        "fwd": (lib.invrope_postmix_fwd, (O.data_ptr(), M.data_ptr(), Y.data_ptr(), c.sq, c.nh, c.nope, c.pe,
+                                          c.pos0, c.theta, stream)),
+        "bwd": (lib.invrope_postmix_bwd, (dY.data_ptr(), O.data_ptr(), M.data_ptr(), dO.data_ptr(), dM.data_ptr(),
+                                          ws.data_ptr(), ws_bytes, c.sq, c.nh, c.nope, c.pe, c.pos0, c.theta,
+                                          stream)),
+    }
+    if idx is not None:
+        argsets["remap"] = (lib.kv_idx_local_to_global, (idx.data_ptr(), out.data_ptr(), idx.shape[0],
+                                                         idx.shape[1], R.sq, R.seqlen_kv, stream))
+    for op in ops:
+        fn, a = argsets[op]
+        for _ in range(10):
+            assert fn(*a) == 0
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n):
+            fn(*a)
+        t1 = time.perf_counter()
+        torch.cuda.synchronize()
+        # the ctypes call itself, on a C-ABI function that returns at once
+        t2 = time.perf_counter()
+        for _ in range(n):
+            lib.invrope_last_cuda_error()
+        t3 = time.perf_counter()
+        print(f"{c.name} {op}: host {1e6 * (t1 - t0) / n:.2f} us per call over {n} enqueues "
+              f"(ctypes round trip alone {1e6 * (t3 - t2) / n:.2f} us)")
 
 
 if __name__ == "__main__":

@@ -56,6 +56,27 @@ def assert_dm_close(gpu: np.ndarray, ref: np.ndarray, what="dM"):
     return rel
 
 
+def compare_all_rows(O, dY, M, Y, dO, positions, nope, pe, theta, block=512, group_size=None):
+    """Y and dO of the CUDA path against the oracle on every row, ``block``
+    rows at a time (host memory stays bounded); ``positions`` holds the
+    absolute position of every row. With ``group_size`` the mix is grouped."""
+    sq = O.shape[0]
+    Oc, dYc, Yc, dOc = (t.detach().cpu() for t in (O, dY, Y, dO))
+    M64 = f64(M)
+    for s0 in range(0, sq, block):
+        s1 = min(sq, s0 + block)
+        O_b, dY_b = f64(Oc[s0:s1]), f64(dYc[s0:s1])
+        pos = positions[s0:s1]
+        if group_size is None:
+            Y_ref = oracle.postmix_fwd(O_b, M64, pos, nope, pe, theta)
+            dO_ref = oracle.postmix_bwd_dO(dY_b, M64, pos, nope, pe, theta)
+        else:
+            Y_ref = oracle.postmix_fwd_grouped(O_b, M64, pos, nope, pe, theta)
+            dO_ref = oracle.postmix_bwd_grouped_dO(dY_b, M64, pos, nope, pe, theta)
+        assert_bf16_close(f64(Yc[s0:s1]), Y_ref, f"Y rows {s0}..{s1 - 1}")
+        assert_bf16_close(f64(dOc[s0:s1]), dO_ref, f"dO rows {s0}..{s1 - 1}")
+
+
 def oracle_fwd_rows(O_cpu64, M64, rows, pos0, nope, pe, theta):
     """Oracle Y for the given rows (positions pos0 + rows)."""
     pos = pos0 + np.asarray(rows, dtype=np.int64)

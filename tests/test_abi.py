@@ -39,7 +39,8 @@ def test_header_declares_the_expected_entry_points():
         "invrope_last_cuda_error", "invrope_postmix_bwd", "invrope_postmix_bwd_workspace_bytes",
         "invrope_postmix_bwd_noalloc", "invrope_postmix_fwd", "invrope_status_string",
         "invrope_take_device_fault", "invrope_watchdog_selftest", "kv_idx_local_to_global",
-        "invrope_postmix_fwd_ex", "invrope_postmix_bwd_ex", "kv_idx_local_to_global_i64"])
+        "invrope_postmix_fwd_ex", "invrope_postmix_bwd_ex", "kv_idx_local_to_global_i64",
+        "invrope_debug_occupy_next_slot"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -72,12 +73,31 @@ FAKE = 0x10000  # never dereferenced: every call below is rejected on the host
     (8, 4, 48, 16, 0, 0.0, INVALID),         # theta <= 0
     (8, 4, 48, 16, 0, float("inf"), INVALID),
     (8, 129, 448, 64, 0, 1e4, UNSUPPORTED),  # more than 128 heads
-    (8, 4, 40, 32, 0, 1e4, UNSUPPORTED),     # pe straddles a 64-channel block
-    (2**30, 4, 448, 64, 0, 1e4, UNSUPPORTED),  # sq * nh >= 2^31
+    (2**30, 4, 448, 64, 0, 1e4, UNSUPPORTED),  # sq * nh >= 2^31: beyond 32-bit row coordinates
 ])
 def test_fwd_rejects_bad_shapes(lib, sq, nh, nope, pe, pos0, theta, want):
     st = lib.invrope_postmix_fwd(FAKE, FAKE, FAKE * 2, sq, nh, nope, pe, pos0, theta, None)
     assert st == want
+
+
+@pytest.mark.parametrize("nh,nope,pe", [
+    (64, 480, 64),   # pe block across a 64-channel boundary
+    (16, 40, 32),
+    (128, 96, 64),
+    (3, 120, 16),
+    (5, 0, 512),     # every channel rotated, 256 pairs
+    (6, 60, 100),    # nope and pe/2 not multiples of 8
+    (64, 384, 128),  # pe wider than 64
+    (1, 6, 2),
+])
+def test_every_pe_placement_passes_the_shape_checks(lib, nh, nope, pe):
+    """Any even pe >= 2 at any offset is a supported shape: the host checks
+    pass, and without a GPU the call stops at the device check."""
+    a = [k << 32 for k in range(1, 7)]  # far apart: no overlap
+    for st in (lib.invrope_postmix_fwd(a[0], a[1], a[2], 8, nh, nope, pe, 0, 1e4, None),
+               lib.invrope_postmix_bwd(a[0], a[1], a[2], a[3], a[4], a[5], 1 << 24,
+                                       8, nh, nope, pe, 0, 1e4, None)):
+        assert st not in (INVALID, UNSUPPORTED), st
 
 
 def test_fwd_rejects_null_and_misaligned_pointers(lib):
@@ -132,7 +152,7 @@ def test_fwd_ex_with_no_rows_is_a_no_op(lib):
 def test_workspace_query_is_zero_for_invalid_shapes(lib):
     assert lib.invrope_postmix_bwd_workspace_bytes(8, 0, 448, 64) == 0
     assert lib.invrope_postmix_bwd_workspace_bytes(8, 4, 448, 63) == 0
-    assert lib.invrope_postmix_bwd_workspace_bytes(8, 4, 40, 32) == 0
+    assert lib.invrope_postmix_bwd_workspace_bytes(8, 129, 448, 64) == 0
 
 
 @pytest.mark.parametrize("rows,topk,sq,skv,want", [

@@ -22,7 +22,8 @@ SCRIPT = textwrap.dedent("""
     from partial_inverse_rope_gb300 import inputs as W
 
     shapes = [(128, 4, 48, 16), (37, 3, 56, 8), (257, 64, 448, 64), (301, 64, 480, 32),
-              (70, 100, 448, 64), (33, 128, 448, 64), (65, 1, 448, 64), (40, 128, 64, 64)]
+              (70, 100, 448, 64), (33, 128, 448, 64), (65, 1, 448, 64), (40, 128, 64, 64),
+              (300, 64, 480, 64), (77, 128, 96, 64), (33, 6, 60, 100), (45, 5, 0, 512), (70, 12, 62, 10)]
     for sq, nh, nope, pe in shapes:
         O = W.normal_bf16((sq, nh, nope + pe), 1, "cuda")
         dY = W.normal_bf16((sq, nh, nope + pe), 2, "cuda")

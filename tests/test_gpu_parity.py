@@ -9,8 +9,7 @@ import torch
 import oracle
 import partial_inverse_rope_gb300 as ir
 from partial_inverse_rope_gb300 import binding
-from gpu_helpers import (assert_bf16_close, assert_dm_close, ensure_built, f64, make_inputs,
-                         sample_rows)
+from gpu_helpers import assert_bf16_close, assert_dm_close, compare_all_rows, ensure_built, f64, make_inputs
 from partial_inverse_rope_gb300 import inputs as W
 
 pytestmark = pytest.mark.gpu
@@ -72,6 +71,19 @@ SHAPES = [
     (515, 48, 448, 64, 2, 1e4),       # nh = 48: 2 positions, R = 96, block-diagonal backward mix
     (200, 24, 100, 28, 4, 1e4),       # pe/2 = 14 (scalar rotation path), pe block inside chunk 1
     (90, 128, 510, 2, 6, 1e4),        # 128 heads, the smallest pe (one pair) at the end of d = 512
+    # the pe block across a 64-channel boundary, or wider than 64: pair blocks of
+    # the general tiling (nope tiles clipped at channel nope, pairs stored directly)
+    (300, 64, 480, 64, 9, 1e4),       # 448 + 64 shifted by 32 channels
+    (100, 16, 40, 32, 3, 1e4),
+    (77, 128, 96, 64, 5, 1e4),        # 128 heads: one position per tile
+    (50, 3, 120, 16, 2, 1e4),
+    (64, 8, 384, 128, 7, 1e4),        # pe = 128: two pair blocks
+    (45, 5, 0, 512, 11, 1e4),         # every channel rotated, 8 pair blocks
+    (70, 12, 62, 10, 3, 1e4),         # nope % 8 != 0 and pe / 2 odd: unaligned pairs
+    (33, 6, 60, 100, 4, 1e4),         # 50 pairs from channel 60: unaligned, two pair blocks
+    (20, 64, 2, 254, 1, 1e4),         # 127 pairs, 64 heads
+    (40, 7, 220, 76, 2**31 + 5, 5e5), # unaligned pairs, positions beyond 2^31, another base
+    (131, 100, 448, 72, 8, 1e4),      # 36 pairs (a 4-pair second block), 100 heads
 ]
 
 
@@ -95,48 +107,38 @@ def test_sweep_nh3_config():
     _full_check(c.sq, c.nh, c.nope, c.pe, c.pos0, c.theta, seed=c.seed)
 
 
-def _large_check(c, rows_per_tile, n_random=48):
-    """Full-size run; Y/dO compared on sampled rows, dM against the full oracle sum."""
+def _large_check(c):
+    """Full-size run: every row of Y and dO against the oracle (in blocks of
+    rows, to bound host memory), dM against the full oracle sum."""
     O, dY, M = W.postmix_inputs(c, device="cuda")
     Y = ir.invrope_postmix_fwd(O, M, c.pos0, c.nope, c.pe, c.theta)
     dO, dM = ir.invrope_postmix_bwd(dY, O, M, c.pos0, c.nope, c.pe, c.theta)
     torch.cuda.synchronize()
-    rows = sample_rows(c.sq, rows_per_tile, n_random)
-    M64 = f64(M)
-    pos = c.pos0 + rows
-    O_s, dY_s = f64(O[rows]), f64(dY[rows])
-    Y_ref = oracle.postmix_fwd(O_s, M64, pos, c.nope, c.pe, c.theta)
-    dO_ref, _ = oracle.postmix_bwd(dY_s, O_s, M64, pos, c.nope, c.pe, c.theta)
-    assert_bf16_close(f64(Y[rows]), Y_ref, "Y (sampled rows)")
-    assert_bf16_close(f64(dO[rows]), dO_ref, "dO (sampled rows)")
+    all_pos = np.arange(c.pos0, c.pos0 + c.sq, dtype=np.int64)
+    compare_all_rows(O, dY, M, Y, dO, all_pos, c.nope, c.pe, c.theta)
     O32 = O.cpu().to(torch.float32).numpy()
     dY32 = dY.cpu().to(torch.float32).numpy()
-    all_pos = np.arange(c.pos0, c.pos0 + c.sq, dtype=np.int64)
     dM_ref = oracle.postmix_bwd_dM(dY32, O32, all_pos, c.nope, c.pe, c.theta)
     return assert_dm_close(f64(dM), dM_ref)
 
 
 def test_production_shard_full_size():
-    _large_check(W.PROD, 2)
+    _large_check(W.PROD)
 
 
 def test_sweep_nh128_full_size():
-    _large_check(W.SWEEP_NH128, 1)
+    _large_check(W.SWEEP_NH128)
 
 
 def test_many_rows_small_channels():
-    """2^27 + rows of the [sq*nh, d] view: large row coordinates, sampled parity."""
+    """2^27 + rows of the [sq*nh, d] view: large row coordinates, every row compared."""
     sq, nh, nope, pe = 2_097_159, 64, 0, 8
     O, dY, M = make_inputs(sq, nh, nope, pe, seed=5)
     Y = ir.invrope_postmix_fwd(O, M, 9, nope, pe, 1e4)
     dO, _ = ir.invrope_postmix_bwd(dY, O, M, 9, nope, pe, 1e4)
     torch.cuda.synchronize()
-    rows = sample_rows(sq, 2, 32)
-    pos = 9 + rows
-    M64 = f64(M)
-    assert_bf16_close(f64(Y[rows]), oracle.postmix_fwd(f64(O[rows]), M64, pos, nope, pe, 1e4), "Y")
-    dO_ref, _ = oracle.postmix_bwd(f64(dY[rows]), f64(O[rows]), M64, pos, nope, pe, 1e4)
-    assert_bf16_close(f64(dO[rows]), dO_ref, "dO")
+    compare_all_rows(O, dY, M, Y, dO, np.arange(9, 9 + sq, dtype=np.int64), nope, pe, 1e4,
+                     block=65536)
 
 
 # ------------------------------------------------------------------ exact special cases
@@ -182,7 +184,7 @@ def test_bitwise_repeatable():
         assert torch.equal(dM, outs[0][2])
 
 
-@pytest.mark.parametrize("nh,nope,pe", [(64, 0, 64), (16, 0, 32), (64, 8, 56)])
+@pytest.mark.parametrize("nh,nope,pe", [(64, 0, 64), (16, 0, 32), (64, 8, 56), (16, 0, 128), (32, 4, 60)])
 def test_every_tile_a_pe_tile_repeated(nh, nope, pe):
     """One channel tile, so every backward tile carries pe channels and the
     hand-offs to the transform warps come back to back; many calls in a row
@@ -196,10 +198,9 @@ def test_every_tile_a_pe_tile_repeated(nh, nope, pe):
         assert torch.equal(dM, dM0)
     torch.cuda.synchronize()
     assert ir.invrope_take_device_fault() == 0
-    rows = sample_rows(sq, 128 // nh, 16)
-    dO_ref, _ = oracle.postmix_bwd(f64(dY[rows]), f64(O[rows]), f64(M), 3 + rows, nope, pe, 1e4)
-    assert_bf16_close(f64(dO0[rows]), dO_ref, "dO")
-    dM_ref = oracle.postmix_bwd_dM(f64(dY), f64(O), np.arange(3, 3 + sq, dtype=np.int64), nope, pe, 1e4)
+    dO_ref, dM_ref = oracle.postmix_bwd(f64(dY), f64(O), f64(M), np.arange(3, 3 + sq, dtype=np.int64), nope, pe,
+                                        1e4)
+    assert_bf16_close(f64(dO0), dO_ref, "dO")
     assert_dm_close(f64(dM0), dM_ref)
 
 

@@ -1,14 +1,17 @@
 """The library's calls on several streams at once, and inside a captured CUDA
 graph: both must give the same bits as plain calls on one stream. The forward
-claims tiles from a per-launch counter slot and the backward's reduction is a
-programmatic dependent launch, so these are the paths that concurrency and
-capture could disturb. Needs a GB300 (sm_103a)."""
+and the remap claim work from a per-launch counter slot and the backward's
+reduction is a programmatic dependent launch, so these are the paths that
+concurrency and capture could disturb. A launch that finds its slot held by
+another launch must report it rather than share the counter. Needs a GB300
+(sm_103a)."""
 
 import pytest
 import torch
 
 import partial_inverse_rope_gb300 as ir
 from gpu_helpers import ensure_built, make_inputs
+from partial_inverse_rope_gb300 import binding
 
 pytestmark = pytest.mark.gpu
 
@@ -90,3 +93,68 @@ def test_graph_replay_matches_eager():
         graph.replay()
         torch.cuda.synchronize()
         _same(eager, o)
+
+
+def test_graph_replay_beside_many_eager_launches():
+    """A captured forward and remap keep their (capture) counter slots on every
+    replay; eager launches on another stream cycle through the eager slots at
+    the same time, more than 256 of them, and never meet the replay's slot."""
+    case = _case(41)
+    O, dY, M, idx = case
+    _, _, nope, pe = SHAPE
+    eager = _outputs(O, idx)
+    _run(case, eager)
+    torch.cuda.synchronize()
+    o = _outputs(O, idx)
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            ir.invrope_postmix_fwd(O, M, 7, nope, pe, Y=o["Y"])
+            ir.kv_idx_local_to_global(idx, 512, 4096, out=o["out"])
+    torch.cuda.synchronize()
+    other = torch.cuda.Stream()
+    Ys = [torch.empty_like(O) for _ in range(2)]
+    outs = [torch.empty_like(idx) for _ in range(2)]
+    for _ in range(3):
+        o["Y"].zero_()
+        o["out"].zero_()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            graph.replay()
+        with torch.cuda.stream(other):
+            for k in range(300):
+                ir.invrope_postmix_fwd(O, M, 7, nope, pe, Y=Ys[k % 2], stream=other)
+                ir.kv_idx_local_to_global(idx, 512, 4096, out=outs[k % 2], stream=other)
+        torch.cuda.synchronize()
+        assert torch.equal(o["Y"], eager["Y"])
+        assert torch.equal(o["out"], eager["out"])
+        assert torch.equal(Ys[1], eager["Y"]) and torch.equal(outs[1], eager["out"])
+    assert ir.invrope_take_device_fault() == 0
+
+
+@pytest.mark.parametrize("which", ["fwd", "remap"])
+def test_busy_slot_is_reported_not_shared(which):
+    """The next launch's counter slot is marked as held by a launch tag that no
+    launch has (a host-side write through the test hook): that launch must
+    claim nothing from it and record the busy-slot code. Taking the fault frees
+    every slot, and the next call gives the bits of a plain call again."""
+    case = _case(43)
+    O, dY, M, idx = case
+    _, _, nope, pe = SHAPE
+
+    def call():
+        if which == "fwd":
+            return ir.invrope_postmix_fwd(O, M, 7, nope, pe)
+        return ir.kv_idx_local_to_global(idx, 512, 4096)
+
+    ref = call()
+    assert ir.invrope_take_device_fault() == 0
+    ir.invrope_debug_occupy_next_slot(which, (1 << 63) + 12345)
+    call()  # finds its slot busy: output undefined
+    want = binding.INVROPE_FAULT_SCHED_BUSY_FWD if which == "fwd" else binding.INVROPE_FAULT_SCHED_BUSY_REMAP
+    assert ir.invrope_take_device_fault() == want
+    for _ in range(3):
+        assert torch.equal(call(), ref)
+    assert ir.invrope_take_device_fault() == 0

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 import partial_inverse_rope_gb300 as ir
-from gpu_helpers import assert_bf16_close, assert_dm_close, ensure_built, f64, sample_rows
+from gpu_helpers import assert_bf16_close, assert_dm_close, compare_all_rows, ensure_built, f64
 from partial_inverse_rope_gb300 import inputs as W
 
 pytestmark = pytest.mark.gpu
@@ -32,6 +32,8 @@ def _inputs(sq, nh, d, seed):
     (101, 6, 3, 56, 8),       # scalar rotation path, ragged rows
     (64, 12, 1, 48, 16),      # gs = 1: each head scaled by its own factor
     (33, 128, 32, 448, 64),
+    (100, 16, 4, 40, 32),     # pe block across a 64-channel boundary (general tiling)
+    (60, 64, 16, 480, 64),
 ])
 def test_grouped_parity(sq, nh, gs, nope, pe):
     O, dY = _inputs(sq, nh, nope + pe, seed=sq + gs)
@@ -89,6 +91,7 @@ def test_one_group_equals_plain_entry_points_bitwise():
     (257, 8, 112, 16, -5000, 5000, 0),          # negative positions
     (99, 5, 56, 8, 2**31 - 4096, 2**31 - 1, 77),  # near the int32 end, plus an offset
     (65, 1, 448, 64, 0, 1 << 20, 3),            # one head, 32 positions per tile
+    (150, 16, 100, 156, -3000, 3000, 5),        # general tiling: 78 pairs from channel 100
 ])
 def test_positions_parity(sq, nh, nope, pe, low, high, pos0):
     O, dY = _inputs(sq, nh, nope + pe, seed=sq)
@@ -118,7 +121,7 @@ def test_contiguous_positions_array_equals_pos0_bitwise():
 
 def test_folded_sequences_full_size():
     """The production shard's token axis holding 4 sequences of 4096 tokens
-    (positions restart per sequence); sampled rows and the full dM."""
+    (positions restart per sequence); every row of Y and dO, and dM."""
     c = W.PROD
     O, dY, M = W.postmix_inputs(c, device="cuda")
     p64 = oracle.positions_batched(4, c.sq // 4, 0)
@@ -126,12 +129,7 @@ def test_folded_sequences_full_size():
     Y = ir.invrope_postmix_fwd_ex(O, M, c.nope, c.pe, positions=pos)
     dO, dM = ir.invrope_postmix_bwd_ex(dY, O, M, c.nope, c.pe, positions=pos)
     torch.cuda.synchronize()
-    rows = np.unique(np.concatenate([sample_rows(c.sq, 2, 32), [4095, 4096, 8191, 8192, 12288]]))
-    M64 = f64(M)
-    assert_bf16_close(f64(Y[rows]), oracle.postmix_fwd(f64(O[rows]), M64, p64[rows], c.nope, c.pe, c.theta),
-                      "Y (sampled rows)")
-    dO_ref, _ = oracle.postmix_bwd(f64(dY[rows]), f64(O[rows]), M64, p64[rows], c.nope, c.pe, c.theta)
-    assert_bf16_close(f64(dO[rows]), dO_ref, "dO (sampled rows)")
+    compare_all_rows(O, dY, M, Y, dO, p64, c.nope, c.pe, c.theta)
     dM_ref = oracle.postmix_bwd_dM(dY.cpu().float().numpy(), O.cpu().float().numpy(), p64, c.nope, c.pe,
                                    c.theta)
     assert_dm_close(f64(dM), dM_ref)
