@@ -278,6 +278,7 @@ int kv_idx_local_to_global_i64(const int64_t* idx, int64_t* out,
  */
 #define INVROPE_FAULT_SCHED_BUSY_FWD 0x5C1
 #define INVROPE_FAULT_SCHED_BUSY_REMAP 0x5C2
+#define INVROPE_FAULT_SCHED_BUSY_BWD 0x5C3
 int invrope_take_device_fault(int* fault);
 
 /*

@@ -72,6 +72,7 @@ _SIGNATURES = {
 INVROPE_WATCHDOG_SELFTEST_CODE = 0x60A
 INVROPE_FAULT_SCHED_BUSY_FWD = 0x5C1
 INVROPE_FAULT_SCHED_BUSY_REMAP = 0x5C2
+INVROPE_FAULT_SCHED_BUSY_BWD = 0x5C3
 
 
 class InvropeError(RuntimeError):

@@ -43,6 +43,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -89,7 +90,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;         // bounded waits: 2 s
 // fault codes: role in bits 8-11, barrier kind in bits 0-7
 enum : unsigned { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleTransform = 4, kRoleStore = 5 };
 enum : unsigned { kBarFull = 1, kBarEmpty, kBarAccFull, kBarAccEmpty, kBarXFull, kBarXEmpty,
-                  kBarD2, kBarDone, kBarXGo, kBarOut, kBarM };
+                  kBarD2, kBarDone, kBarXGo, kBarOut, kBarM, kBarSeg, kBarD2Empty };
 
 // WIDE (backward with one position per tile, nh > 64): 128-channel tiles, so
 // each head-mix MMA has N = 128 and a tile needs half as many of them.
@@ -123,9 +124,12 @@ struct KCfg {
   static constexpr int kOffTabXf = kOffTabEpi + kTabBytes;
   static constexpr int kOffFreq = kOffTabXf + (BWD ? kTabBytes : 0);
   static constexpr int kOffBars = kOffFreq + kMaxHalf * 8;
-  static constexpr int kNumBars = 2 * kStages + 2 * kOutBufs + 2 * kNumAcc + 6;
+  // + backward segment ring (4 full, 4 empty) and the D2 hand-back
+  static constexpr int kNumBars = 2 * kStages + 2 * kOutBufs + 2 * kNumAcc + 6 + (BWD ? 9 : 0);
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 192;      // tmem base, abort flag, wait slots, tile ids
+  // tmem base, abort flag, wait slots, tile ids (192 B), backward segment ring
+  // and its broadcast slots (128 B)
+  static constexpr int kSmemBytes = kOffMisc + 192 + (BWD ? 128 : 0);
   static constexpr int kSmemAlloc = kSmemBytes + 1024;   // slack to align the base
   static_assert(kSmemAlloc <= 232448, "shared memory budget");
   static_assert(kNumAcc * NC + (BWD ? 128 : 0) <= kACol, "TMEM budget");
@@ -164,6 +168,12 @@ struct PostmixParams {
   int n_nope_ct;
   int64_t rows;        // sq * nh: rows of the [sq*nh, d] view
   double log2_theta;   // rotary frequencies beyond the first 32 pairs are formed on the device
+  // Backward schedule: CTA c first runs tiles [n_static c / G, n_static (c+1) / G)
+  // into dM partial slot c; the tiles from n_static on form n_tail fixed blocks
+  // (tail_na of tail_ba tiles, then blocks of tail_bb tiles), claimed one at a
+  // time from the launch's counter slot, block b into partial slot G + b.
+  int64_t n_static;
+  int n_tail, tail_na, tail_ba, tail_bb;
 };
 
 // kind 0: a tile of the regular tiling (channels c0 + 64 k, TMA-stored);
@@ -422,6 +432,11 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
   const uint32_t bar_done = bar_x_full + 24;
   const uint32_t bar_x_go = bar_x_full + 32;
   const uint32_t bar_m = bar_x_full + 40;  // M's bulk copy into shared memory
+  // backward: segment ring (full: the producer published segment k; empty: its
+  // four consumers have read it) and D2 handed back by the drain
+  auto bar_seg_full = [&](int k) { return bar_x_full + 48 + 8u * k; };
+  auto bar_seg_empty = [&](int k) { return bar_x_full + 80 + 8u * k; };
+  const uint32_t bar_d2_empty = bar_x_full + 112;
   auto stage_addr = [&](int s) { return base + C::kOffStage + static_cast<uint32_t>(s) * C::kStageBytes; };
   auto out_addr = [&](int b) { return base + C::kOffOut + static_cast<uint32_t>(b) * kChunkBytes; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
@@ -438,6 +453,12 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
   volatile int* ob_tile = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 128);    // [OB]
   volatile int* ob_chunk = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 160);   // [OB]
   static_assert(S <= 8 && NA <= 8 && OB <= 8, "tile-id slots");
+  // backward segment ring: entry k = {t0, t1, slot} (t0 < 0: no more segments),
+  // and per-group broadcast slots {ok, t0, t1, slot} for the epilogue and the
+  // transform warps (two each, alternating by segment parity)
+  volatile int* seg_ring = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 192);   // [4][4]
+  volatile int* seg_bc_epi = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 256);  // [2][4]
+  volatile int* seg_bc_xf = reinterpret_cast<volatile int*>(gbase + C::kOffMisc + 288);   // [2][4]
   uint64_t* F = reinterpret_cast<uint64_t*>(gbase + C::kOffFreq);
   const int half = p.pe >> 1;
   // Accumulator ring: NA accumulators of NC columns, or 2 of 128 columns for the
@@ -453,7 +474,8 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
   // thread 0 (the TMA producer) issues the slot acquisition first; its result
   // is needed only at the end of the barrier set-up
   bool sched_mine = false;
-  if (!BWD && threadIdx.x == 0) sched_mine = sched_acquire(p.sched, launch_tag());
+  const bool use_sched = !BWD || p.n_tail > 0;
+  if (use_sched && threadIdx.x == 0) sched_mine = sched_acquire(p.sched, launch_tag());
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(bar_full(s), 1);
@@ -473,10 +495,18 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
     ptx::mbar_init(bar_done, 1);
     ptx::mbar_init(bar_x_go, 1);
     ptx::mbar_init(bar_m, 1);
+    if constexpr (BWD) {
+      for (int k = 0; k < 4; ++k) {
+        ptx::mbar_init(bar_seg_full(k), 1);
+        ptx::mbar_init(bar_seg_empty(k), 4);  // MMA thread, epilogue, store warp, transform warps
+      }
+      ptx::mbar_init(bar_d2_empty, 128);
+    }
     *abort_flag = 0;
-    // forward: take the launch's counter slot; if another launch still holds
-    // it, claim nothing from it and wind down (outputs undefined, fault recorded)
-    if (!BWD && !sched_mine) record_fault(INVROPE_FAULT_SCHED_BUSY_FWD, abort_flag);
+    // take the launch's counter slot; if another launch still holds it, claim
+    // nothing from it and wind down (outputs undefined, fault recorded)
+    if (use_sched && !sched_mine)
+      record_fault(BWD ? INVROPE_FAULT_SCHED_BUSY_BWD : INVROPE_FAULT_SCHED_BUSY_FWD, abort_flag);
     ptx::fence_mbar_init();
     // forward: M goes out first, ahead of every tile load; the A build waits on it
     if (!BWD && p.m_bulk) {
@@ -517,8 +547,60 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const int64_t G = gridDim.x;
-  const int64_t t_begin = p.n_tiles * blockIdx.x / G;
-  const int64_t t_end = p.n_tiles * (blockIdx.x + 1) / G;
+  // forward: unused; backward: this CTA's static share of the first n_static tiles
+  const int64_t t_begin = p.n_static * blockIdx.x / G;
+  const int64_t t_end = p.n_static * (blockIdx.x + 1) / G;
+
+  // Backward segments, in the order every role runs them: segment 0 is the
+  // static share (dM partial slot blockIdx.x), then the tail blocks this CTA
+  // claimed (slot G + b). The producer publishes them through a 4-entry ring.
+  auto tail_block = [&](uint32_t b, int64_t& t0, int64_t& t1) {
+    const uint32_t na = static_cast<uint32_t>(p.tail_na);
+    t0 = b < na ? p.n_static + static_cast<int64_t>(b) * p.tail_ba
+                : p.n_static + static_cast<int64_t>(na) * p.tail_ba + static_cast<int64_t>(b - na) * p.tail_bb;
+    t1 = t0 + (b < na ? p.tail_ba : p.tail_bb);
+    if (t1 > p.n_tiles) t1 = p.n_tiles;
+  };
+  auto seg_publish = [&](uint32_t k, int64_t t0, int64_t t1, int slot) -> bool {
+    const int e = static_cast<int>(k & 3u);
+    if (!wait_bar(bar_seg_empty(e), ((k >> 2) & 1u) ^ 1u, abort_flag, (kRoleProducer << 8) | kBarSeg))
+      return false;
+    seg_ring[4 * e] = static_cast<int>(t0);
+    seg_ring[4 * e + 1] = static_cast<int>(t1);
+    seg_ring[4 * e + 2] = slot;
+    ptx::mbar_arrive(bar_seg_full(e));  // release: the entry is visible to whoever sees the phase
+    return true;
+  };
+  // one consumer thread reads segment k (t0 < 0: no more segments)
+  auto seg_read = [&](uint32_t k, int64_t& t0, int64_t& t1, int& slot, unsigned code) -> bool {
+    const int e = static_cast<int>(k & 3u);
+    if (!wait_bar(bar_seg_full(e), (k >> 2) & 1u, abort_flag, code)) return false;
+    t0 = seg_ring[4 * e];
+    t1 = seg_ring[4 * e + 1];
+    slot = seg_ring[4 * e + 2];
+    ptx::mbar_arrive(bar_seg_empty(e));
+    return true;
+  };
+  // a 128-thread group: its leader reads, the group learns it through bc[k & 1]
+  auto seg_read_group = [&](uint32_t k, int64_t& t0, int64_t& t1, int& slot, unsigned code, bool leader,
+                            volatile int* bc, uint32_t bar_id) -> bool {
+    volatile int* b = bc + 4 * (k & 1u);
+    if (leader) {
+      int64_t a0 = 0, a1 = 0;
+      int sl = 0;
+      const bool ok = seg_read(k, a0, a1, sl, code);
+      b[0] = ok ? 1 : 0;
+      b[1] = static_cast<int>(a0);
+      b[2] = static_cast<int>(a1);
+      b[3] = sl;
+    }
+    ptx::named_bar_sync(bar_id, 128);
+    if (!b[0]) return false;
+    t0 = b[1];
+    t1 = b[2];
+    slot = b[3];
+    return true;
+  };
 
   // The producer starts streaming right away; meanwhile every other warp
   // builds A in TMEM and (backward) clears X_lo, then they meet at named
@@ -621,12 +703,34 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
       // forward: the first tile is the block index, later ones are claimed
-      // from the launch's counter, one claim ahead
+      // from the launch's counter, one claim ahead. Backward: the static share,
+      // then tail blocks claimed one segment ahead, each segment published to
+      // the other roles before its first tile is loaded.
       int64_t t_next = BWD ? t_begin : static_cast<int64_t>(blockIdx.x);
-      for (uint32_t i = 0;; ++i) {
+      int64_t seg_end = t_end;
+      uint32_t seg_k = 0;
+      uint32_t claim = 0xffffffffu;
+      bool run = true;
+      if constexpr (BWD) {
+        run = !*abort_flag && seg_publish(0, t_begin, t_end, static_cast<int>(blockIdx.x));
+        if (run && p.n_tail > 0) claim = atomicAdd(&p.sched->next, 1u);
+      }
+      for (uint32_t i = 0; run; ++i) {
         const int st = static_cast<int>(i % S);
         const uint32_t ph = (i / S) & 1u;
-        if (BWD && t_next >= t_end) break;
+        if (BWD && t_next >= seg_end) {
+          ++seg_k;
+          if (claim >= static_cast<uint32_t>(p.n_tail)) {
+            seg_publish(seg_k, -1, -1, -1);
+            break;
+          }
+          int64_t a0 = 0, a1 = 0;
+          tail_block(claim, a0, a1);
+          if (!seg_publish(seg_k, a0, a1, static_cast<int>(G + claim))) break;
+          t_next = a0;
+          seg_end = a1;
+          claim = atomicAdd(&p.sched->next, 1u);
+        }
         if (*abort_flag) break;
         if (!wait_bar(bar_empty(st), ph ^ 1u, abort_flag, (kRoleProducer << 8) | kBarEmpty)) break;
         const int64_t t = t_next;
@@ -666,8 +770,16 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
       const uint32_t nks = static_cast<uint32_t>((p.R + 15) / 16);
       uint32_t d2_started = 0;
       int npe = 0;
+      // D2 of a new segment may start only once the drain has read the last one out
+      bool d2_wait = false;
+      uint32_t d2_par = 0;
       // D2 += dY_tile * X_tile^T (both K-major, K = channels), plus dY_pe * X_lo^T on a pe tile
-      auto dm_chain = [&](int st, const Tile& x) {
+      auto dm_chain = [&](int st, const Tile& x) -> bool {
+        if (d2_wait) {
+          if (!wait_bar(bar_d2_empty, d2_par, abort_flag, (kRoleMma << 8) | kBarD2Empty)) return false;
+          ptx::tc_fence_after();
+          d2_wait = false;
+        }
         const uint32_t sa = stage_addr(st);
         const uint32_t d2 = tmem_base + C::kD2Col;
         const uint32_t idesc_dm = ptx::idesc_bf16_f32(128, 128, false, false);
@@ -692,6 +804,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
               ptx::tc_mma_ss(d2, ad, bd, idesc_dm, 1);
             }
         }
+        return true;
       };
       // the pe tile whose dM chain is still to be issued (stage, tile)
       int pend_st = -1;
@@ -700,21 +813,41 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
         if (!wait_bar(bar_x_full, static_cast<uint32_t>(npe & 1), abort_flag, (kRoleMma << 8) | kBarXFull))
           return false;
         ptx::tc_fence_after();
-        dm_chain(pend_st, pend_x);
+        if (!dm_chain(pend_st, pend_x)) return false;
         ptx::tc_commit(bar_empty(pend_st));
         ptx::tc_commit(bar_x_empty);
         ++npe;
         pend_st = -1;
         return true;
       };
-      for (uint32_t i = 0;; ++i) {
+      // Backward: an outer loop over the segments, the per-tile loop within
+      // a segment; the segment changes stay out of the per-tile loop, which is
+      // the MMA thread's hot code. Forward: one pass of the per-tile loop.
+      uint32_t seg_k = 0, i = 0;
+      for (;;) {
+        int64_t s_t = 0, s_t1 = 0;
+        if constexpr (BWD) {
+          int s_slot = 0;
+          if (!seg_read(seg_k, s_t, s_t1, s_slot, (kRoleMma << 8) | kBarSeg)) break;
+          ++seg_k;
+          if (s_t < 0) break;
+        }
+        bool seg_done = false;
+      for (;; ++i) {
         const int st = static_cast<int>(i % S);
         const uint32_t ph = (i / S) & 1u;
         const int acc = acc_of(i);
         const uint32_t aph = acc_phase(i);
-        if (BWD && t_begin + i >= t_end) break;
+        int64_t t = 0;
+        if constexpr (BWD) {
+          if (s_t >= s_t1) {
+            seg_done = true;
+            break;
+          }
+          t = s_t++;
+        }
         if (!wait_bar(bar_full(st), ph, abort_flag, (kRoleMma << 8) | kBarFull)) break;
-        const int64_t t = BWD ? t_begin + i : static_cast<int64_t>(stage_tile[st]);
+        if (!BWD) t = static_cast<int64_t>(stage_tile[st]);
         if (!BWD && t < 0) {
           // pass the end of the tile stream on to the epilogue
           if (!wait_bar(bar_acc_empty(acc), aph ^ 1u, abort_flag, (kRoleMma << 8) | kBarAccEmpty)) break;
@@ -766,7 +899,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
         // the input ring keep moving while X is formed. The issue order is fixed
         // by the tile sequence alone, so D2 (and dM) stay reproducible.
         if (!x.has_pe) {
-          dm_chain(st, x);
+          if (!dm_chain(st, x)) break;
           ptx::tc_commit(bar_empty(st));
         }
         if (pend_st >= 0 && !flush_pending()) break;
@@ -776,8 +909,16 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
           pend_x = x;
         }
       }
-      if (BWD && pend_st >= 0) flush_pending();
-      if (BWD) ptx::tc_commit(bar_d2);
+        if (!seg_done) break;  // forward: the end of the tile stream; else a wait gave up
+        // The segment is issued: its last pe tile's dM chain goes out, then D2
+        // is handed to the drain (transform warps) once every MMA so far
+        // completes; the next segment's D2 starts from zero.
+        if (pend_st >= 0 && !flush_pending()) break;
+        ptx::tc_commit(bar_d2);
+        d2_wait = true;
+        d2_par = (seg_k - 1) & 1u;
+        d2_started = 0;
+      }
       // every MMA issued must complete before TMEM is freed, abort or not
       ptx::tc_commit(bar_done);
       wait_bar_noabort(bar_done, 0);
@@ -795,15 +936,31 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
     const float sgn = BWD ? 1.f : -1.f;  // rope (+a) for dO, inverse rope (-a) for Y
     uint32_t n = 0;  // output chunk counter (output ring position)
     bool ok = true;
-    // backward: the next tile's (row tile, channel tile), advanced without a division
+    // backward: the next tile's (row tile, channel tile), advanced without a
+    // division within a segment [s_t, s_t1); the segments in an outer loop
     int e_rt = 0, e_ct = 0;
-    if (BWD) {
-      const Tile x0 = decode_tile<BWD, WIDE>(p, t_begin);
-      e_rt = x0.rt;
-      e_ct = x0.ct;
-    }
-    for (uint32_t i = 0; ok; ++i) {
-      if (BWD && t_begin + i >= t_end) break;
+    uint32_t seg_k = 0, i = 0;
+    for (;;) {
+      int64_t s_t = 0, s_t1 = 0;
+      if constexpr (BWD) {
+        int sl = 0;
+        if (!seg_read_group(seg_k, s_t, s_t1, sl, (kRoleEpilogue << 8) | kBarSeg, e == 0, seg_bc_epi, 1)) break;
+        ++seg_k;
+        if (s_t < 0) break;
+        const Tile x0 = decode_tile<BWD, WIDE>(p, s_t);
+        e_rt = x0.rt;
+        e_ct = x0.ct;
+      }
+      bool seg_done = false;
+    for (; ok; ++i) {
+      int64_t t = 0;
+      if constexpr (BWD) {
+        if (s_t >= s_t1) {
+          seg_done = true;
+          break;
+        }
+        t = s_t++;
+      }
       const int acc = acc_of(i);
       const uint32_t aph = acc_phase(i);
       if (stk) {
@@ -824,7 +981,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
         break;
       }
       ptx::tc_fence_after();
-      const int64_t t = BWD ? t_begin + i : static_cast<int64_t>(acc_tile[acc]);
+      if (!BWD) t = static_cast<int64_t>(acc_tile[acc]);
       if (!BWD && t < 0) {
         // pass the end of the tile stream on to the store warp
         const int b = static_cast<int>(n % OB);
@@ -1108,61 +1265,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
         ptx::mbar_arrive(bar_acc_empty(acc));
       }
     }
-    if (BWD && ok) {
-      // This CTA's dM share: the sum of the diagonal nh x nh blocks of D2. The
-      // input ring is free once every MMA has completed.
-      if (group_wait(bar_d2, 0, abort_flag, (kRoleEpilogue << 8) | kBarD2, e == 0, slot_d2, 1)) {
-        ptx::tc_fence_after();
-        if (p.P == 1) {
-          // one position per tile: row r's D2 row is its partial row, straight from TMEM
-          float* dst = p.ws + (static_cast<int64_t>(blockIdx.x) * p.R + r) * p.nh;
-          for (int j0 = 0; j0 < 128; j0 += 32) {
-            uint32_t v[32];
-            ptx::tmem_ld_x32(tmem_base + lane_addr + C::kD2Col + j0, v);
-            ptx::tmem_ld_wait(v);
-            if (row_ok && j0 < p.nh) {
-              if (j0 + 32 <= p.nh && ((p.nh & 3) == 0)) {
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                  *reinterpret_cast<float4*>(dst + j0 + 4 * u) =
-                      make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                                  __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
-              } else {
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj)
-                  if (j0 + jj < p.nh) dst[j0 + jj] = __uint_as_float(v[jj]);
-              }
-            }
-          }
-        } else {
-          // red[h * (R + 1) + r] = D2[r][pl*nh + h]: consecutive rows -> consecutive
-          // words; the odd row stride keeps the transposed reads below conflict-free
-          float* red = reinterpret_cast<float*>(gbase + C::kOffStage);
-          const int rs = p.R + 1;
-          const int lo = pl * p.nh;
-          for (int j0 = 0; j0 < 128; j0 += 32) {
-            uint32_t v[32];
-            ptx::tmem_ld_x32(tmem_base + lane_addr + C::kD2Col + j0, v);
-            ptx::tmem_ld_wait(v);
-            if (row_ok) {
-#pragma unroll
-              for (int jj = 0; jj < 32; ++jj) {
-                const int j = j0 + jj;
-                if (j >= lo && j < lo + p.nh) red[(j - lo) * rs + r] = __uint_as_float(v[jj]);
-              }
-            }
-          }
-          ptx::named_bar_sync(1, 128);
-          const int nn = p.nh * p.nh;
-          // consecutive threads take consecutive h: coalesced partial rows
-          for (int idx = e; idx < nn; idx += 128) {
-            const int g = idx / p.nh, h = idx - g * p.nh;
-            float s = 0.f;
-            for (int q = 0; q < p.P; ++q) s += red[h * rs + q * p.nh + g];
-            p.ws[static_cast<int64_t>(blockIdx.x) * nn + g * p.nh + h] = s;
-          }
-        }
-      }
+      if (!seg_done) break;
     }
   } else if (warp == C::kWarpStore) {
     // ---------------------------------------------------------- TMA store (output ring)
@@ -1170,9 +1273,25 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
       constexpr int kIn = C::kOutInflight;
       uint32_t n = 0;
       bool ok = true;
-      for (uint32_t i = 0; ok; ++i) {
-        if (BWD && t_begin + i >= t_end) break;
-        const int64_t tb = t_begin + i;
+      uint32_t seg_k = 0;
+      for (;;) {
+        int64_t s_t = 0, s_t1 = 0;
+        if constexpr (BWD) {
+          int sl = 0;
+          if (!seg_read(seg_k, s_t, s_t1, sl, (kRoleStore << 8) | kBarSeg)) break;
+          ++seg_k;
+          if (s_t < 0) break;
+        }
+        bool seg_done = false;
+      for (; ok;) {
+        int64_t tb = 0;
+        if constexpr (BWD) {
+          if (s_t >= s_t1) {
+            seg_done = true;
+            break;
+          }
+          tb = s_t++;
+        }
         // forward: one chunk per hand-off; backward: every box of a tile, none
         // of a general pair block (stored directly by the epilogue)
         int nk = 1;
@@ -1204,17 +1323,139 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
           }
         }
       }
+        if (!seg_done) break;
+      }
       ptx::bulk_wait<0>();
     }
     __syncwarp();
   } else {
     // ---------------------------------------------------------- X = invrope(O) on the pe chunk (bwd)
-    if (BWD) {
+    if constexpr (BWD) {
       const int xr = threadIdx.x - 192;
       float2* tab = reinterpret_cast<float2*>(gbase + C::kOffTabXf);
       int npe = 0;
       uint32_t i = 0;
-      for (int64_t t = t_begin; t < t_end; ++t, ++i) {
+      // D2 of segment k -> dM partial slot `slot`: the diagonal nh x nh blocks
+      // of D2 (one per position of a tile), summed over positions. Row r of D2
+      // (position pl = r / nh, head g) holds its block's row in columns
+      // [pl nh, pl nh + nh). The D2 columns are handed back (bar_d2_empty) as
+      // soon as they are read.
+      auto drain_d2 = [&](uint32_t k, int slot) -> bool {
+        if (!group_wait(bar_d2, k & 1u, abort_flag, (kRoleTransform << 8) | kBarD2, xr == 0, slot_d2, 2))
+          return false;
+        ptx::tc_fence_after();
+        const uint32_t q4 = static_cast<uint32_t>(warp & 3);
+        const int r = static_cast<int>(q4 * 32u) + lane;  // this thread's TMEM lane: D2 row r
+        const uint32_t taddr = tmem_base + ((q4 * 32u) << 16) + C::kD2Col;
+        const bool rok = r < p.R;
+        const int nh = p.nh;
+        const int pl = rok ? r / nh : 0, g = r - pl * nh;
+        const int lo = pl * nh, hi = lo + nh;
+        float* dst = p.ws + static_cast<int64_t>(slot) * nh * nh;
+        if (p.P == 1) {
+          // one position per tile: D2 row r is partial row r
+          for (int j0 = 0; j0 < nh; j0 += 32) {
+            uint32_t v[32];
+            ptx::tmem_ld_x32(taddr + j0, v);
+            ptx::tmem_ld_wait(v);
+            if (!rok) continue;
+            float* drow = dst + static_cast<int64_t>(r) * nh;
+            if (j0 + 32 <= nh && (nh & 3) == 0) {
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                *reinterpret_cast<float4*>(drow + j0 + 4 * u) =
+                    make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+            } else {
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj)
+                if (j0 + jj < nh) drow[j0 + jj] = __uint_as_float(v[jj]);
+            }
+          }
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar_d2_empty);
+        } else if (p.P == 2) {
+          // Position 1's rows park theirs in X_lo (free now: the segment's last
+          // dM chain has completed), row g at g * 64 with column c at c ^ (g & 31)
+          // (conflict-free); position 0's rows add them and write the partial.
+          float* xch = reinterpret_cast<float*>(gbase + C::kOffXlo);
+          for (int j0 = 0; j0 < 128; j0 += 32) {
+            if (!__any_sync(0xffffffffu, rok && pl == 1 && j0 < hi && j0 + 32 > lo)) continue;
+            uint32_t v[32];
+            ptx::tmem_ld_x32(taddr + j0, v);
+            ptx::tmem_ld_wait(v);
+            if (rok && pl == 1) {
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj) {
+                const int j = j0 + jj;
+                if (j >= lo && j < hi) xch[g * 64 + ((j - lo) ^ (g & 31))] = __uint_as_float(v[jj]);
+              }
+            }
+          }
+          ptx::named_bar_sync(2, 128);
+          for (int j0 = 0; j0 < 128; j0 += 32) {
+            if (!__any_sync(0xffffffffu, rok && pl == 0 && j0 < nh)) continue;
+            uint32_t v[32];
+            ptx::tmem_ld_x32(taddr + j0, v);
+            ptx::tmem_ld_wait(v);
+            if (rok && pl == 0) {
+              float* drow = dst + static_cast<int64_t>(g) * nh;
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj) {
+                const int j = j0 + jj;
+                if (j < nh) drow[j] = __uint_as_float(v[jj]) + xch[g * 64 + (j ^ (g & 31))];
+              }
+            }
+          }
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar_d2_empty);
+          ptx::named_bar_sync(2, 128);  // every row has read X_lo
+          // X_lo back to zero: the pe transform writes only its pe columns
+          for (uint32_t o = static_cast<uint32_t>(xr) * 16u; o < static_cast<uint32_t>(C::kXloBytes); o += 128u * 16u)
+            ptx::st_shared_v4(base + C::kOffXlo + o, 0u, 0u, 0u, 0u);
+          ptx::fence_proxy_async_smem();
+        } else {
+          // P > 2 positions per tile: such launches have one segment (no tail),
+          // so this runs after the CTA's last MMA and the input ring is free.
+          // red[h * (R + 1) + r] = D2[r][pl nh + h] (odd row stride: the
+          // transposed reads below are conflict-free), then position sums.
+          float* red = reinterpret_cast<float*>(gbase + C::kOffStage);
+          const int rs = p.R + 1;
+          for (int j0 = 0; j0 < 128; j0 += 32) {
+            uint32_t v[32];
+            ptx::tmem_ld_x32(taddr + j0, v);
+            ptx::tmem_ld_wait(v);
+            if (rok) {
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj) {
+                const int j = j0 + jj;
+                if (j >= lo && j < hi) red[(j - lo) * rs + r] = __uint_as_float(v[jj]);
+              }
+            }
+          }
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar_d2_empty);
+          ptx::named_bar_sync(2, 128);
+          const int nn = nh * nh;
+          // consecutive threads take consecutive h: coalesced partial rows
+          for (int idx = xr; idx < nn; idx += 128) {
+            const int gg = idx / nh, h = idx - gg * nh;
+            float sum = 0.f;
+            for (int q = 0; q < p.P; ++q) sum += red[h * rs + q * nh + gg];
+            dst[idx] = sum;
+          }
+        }
+        return true;
+      };
+      uint32_t seg_k = 0;
+      for (;;) {
+        int64_t s_t0 = 0, s_t1 = 0;
+        int s_slot = 0;
+        if (!seg_read_group(seg_k, s_t0, s_t1, s_slot, (kRoleTransform << 8) | kBarSeg, xr == 0, seg_bc_xf, 2))
+          break;
+        if (s_t0 < 0) break;
+        int64_t t = s_t0;
+      for (; t < s_t1; ++t, ++i) {
         const Tile x = decode_tile<BWD, WIDE>(p, t);
         if (!x.has_pe) continue;
         const int st = static_cast<int>(i % S);
@@ -1367,6 +1608,10 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
         ptx::mbar_arrive(bar_x_full);
         ++npe;
       }
+        if (t < s_t1) break;  // a wait gave up: the CTA is winding down
+        if (!drain_d2(seg_k, s_slot)) break;
+        ++seg_k;
+      }
     }
   }
 
@@ -1382,7 +1627,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::kTmemCols);
   }
-  if (!BWD && threadIdx.x == 0 && sched_mine) sched_release(p.sched, gridDim.x);
+  if (use_sched && threadIdx.x == 0 && sched_mine) sched_release(p.sched, gridDim.x);
 }
 
 // dM[o] = sum of the CTA partials ws[c][src(o)] (each [nh, nh]) in a fixed
@@ -1527,6 +1772,7 @@ struct Shape {
   int64_t n_tiles;
   bool gen;   // general tiling: the pe block does not lie inside one 64-channel box
   bool wide;  // backward: 128-channel tiles (one position per tile, or the general tiling)
+  bool tail_ok = false;  // backward: the kernel can hand out tail blocks
 };
 
 // Validate a postmix shape and lay out its tiles (forward, or backward if bwd).
@@ -1609,8 +1855,50 @@ int occupy_postmix_slot(int device, unsigned long long owner) {
   return err == cudaSuccess ? INVROPE_OK : cuda_fail(err);
 }
 
-// Grid size of the backward kernel (one dM partial per CTA).
+// Grid size of the backward kernel.
 static int64_t bwd_grid(const Shape& s, int sms) { return s.n_tiles < sms ? s.n_tiles : sms; }
+
+// The backward's schedule: each CTA's static share of the first n_static
+// tiles, then n_tail fixed tail blocks handed out one at a time, so that
+// CTAs on SMs that draw more memory bandwidth take more of the tail (per-SM
+// bandwidth differs by several percent). Every static share and every tail
+// block has its own dM partial slot, so dM does not depend on which CTA ran
+// what. A tail needs the drain's position sum to run mid-kernel (at most 2
+// positions per tile) and enough tiles per CTA to be worth it; the partial
+// slots stay within 8 MiB (or twice the static slots).
+struct TailPlan {
+  int64_t n_static = 0;
+  int n_tail = 0, na = 0, ba = 0, bb = 0;
+};
+
+static TailPlan bwd_tail_plan(const Shape& s, int64_t grid, int nh) {
+  TailPlan t;
+  t.n_static = s.n_tiles;
+  const int64_t per = s.n_tiles / (grid > 0 ? grid : 1);
+  const int64_t slot_bytes = static_cast<int64_t>(nh) * nh * 4;
+  if (s.P > 2 || per < 96 || slot_bytes > 16 * 1024) return t;
+  if (!s.tail_ok) return t;
+  const int64_t budget = std::max<int64_t>(int64_t(8) << 20, 2 * grid * slot_bytes);
+  const int64_t max_tail = budget / slot_bytes - grid;
+  if (max_tail < grid) return t;
+  // level A: one block per CTA of ~1/12 of a share; level B: small blocks of
+  // ~1/48 of a share for the end
+  t.ba = static_cast<int>(std::max<int64_t>(4, per / 12));
+  t.bb = static_cast<int>(std::max<int64_t>(2, per / 48));
+  t.na = static_cast<int>(grid);
+  const int64_t nb = std::min<int64_t>(max_tail - grid, grid * 3 / 2);
+  const int64_t tail = static_cast<int64_t>(t.na) * t.ba + nb * t.bb;
+  t.n_static = s.n_tiles - tail;
+  t.n_tail = static_cast<int>(t.na + nb);
+  return t;
+}
+
+// Bytes of dM partials a backward launch writes: one [nh, nh] slot per CTA
+// and per tail block.
+static size_t bwd_partial_bytes(const Shape& s, int64_t grid, int nh) {
+  const TailPlan t = bwd_tail_plan(s, grid, nh);
+  return static_cast<size_t>(grid + t.n_tail) * nh * nh * sizeof(float);
+}
 
 }  // namespace invrope
 
@@ -1669,6 +1957,7 @@ extern "C" int invrope_postmix_fwd_ex(const void* O, const float* M, void* Y, in
   p.n_nope_ct = s.n_nope_ct;
   p.rows = sq * nh;
   p.log2_theta = std::log2(theta);
+  p.n_static = s.n_tiles;
   // M by one bulk copy at kernel start: 16-byte aligned, ungrouped, nh % 64 == 0
   p.m_bulk = (aligned(M, 16) && gs == nh && nh % 64 == 0) ? 1 : 0;
   fill_freq(p.F, pe, theta);
@@ -1688,8 +1977,8 @@ extern "C" size_t invrope_postmix_bwd_workspace_bytes(int64_t sq, int nh, int no
   if (check_shape(sq, nh, nope, pe, true, &s) != INVROPE_OK) return 0;
   DeviceInfo dev;
   if (current_device(&dev) != INVROPE_OK) return 0;
-  const int64_t grid = sq == 0 ? 1 : bwd_grid(s, dev.sms);
-  return static_cast<size_t>(grid) * nh * nh * sizeof(float);
+  if (sq == 0) return static_cast<size_t>(nh) * nh * sizeof(float);
+  return bwd_partial_bytes(s, bwd_grid(s, dev.sms), nh);
 }
 
 extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float* M, void* dO, float* dM,
@@ -1709,7 +1998,8 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
   DeviceInfo dev;
   if ((st = current_device(&dev)) != INVROPE_OK) return st;
   const int64_t grid = sq == 0 ? 0 : bwd_grid(s, dev.sms);
-  const size_t need = static_cast<size_t>(grid == 0 ? 1 : grid) * nh * nh * sizeof(float);
+  const TailPlan tail = grid > 0 ? bwd_tail_plan(s, grid, nh) : TailPlan{};
+  const size_t need = grid == 0 ? static_cast<size_t>(nh) * nh * sizeof(float) : bwd_partial_bytes(s, grid, nh);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return INVROPE_ERR_WORKSPACE;
   const void* outs[3] = {dO, dM, workspace};
   const size_t out_bytes[3] = {tbytes, mbytes, need};
@@ -1753,6 +2043,15 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
     p.rows = sq * nh;
     p.log2_theta = std::log2(theta);
     p.m_bulk = 0;  // the backward reads M from L2 (a bulk copy did not pay off there)
+    p.n_static = tail.n_static;
+    p.n_tail = tail.n_tail;
+    p.tail_na = tail.na;
+    p.tail_ba = tail.ba;
+    p.tail_bb = tail.bb;
+    p.sched = nullptr;
+    if (tail.n_tail > 0 &&
+        (st = slot_take(g_sched_ring, &g_sched, dev.device, cs, &p.sched)) != INVROPE_OK)
+      return st;
     fill_freq(p.F, pe, theta);
     if (wide)
       postmix_kernel<true, true>
@@ -1776,7 +2075,7 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const cudaError_t err = cudaLaunchKernelEx(&cfg, dm_reduce_kernel, static_cast<const float*>(workspace), dM,
-                                             static_cast<int>(grid), nh, gs);
+                                             static_cast<int>(grid + tail.n_tail), nh, gs);
   if (err != cudaSuccess) return cuda_fail(err);
   return check_launch();
 }

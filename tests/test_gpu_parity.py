@@ -204,6 +204,28 @@ def test_every_tile_a_pe_tile_repeated(nh, nope, pe):
     assert_dm_close(f64(dM0), dM_ref)
 
 
+@pytest.mark.parametrize("sq,nh,nope,pe,pos0", [
+    (4096, 64, 448, 64, 16384),   # the stacked mix: static shares plus tail blocks
+    (8192, 64, 480, 64, 7),       # general tiling, 128-channel tiles, two positions per tile
+])
+def test_backward_tail_blocks_exact_and_repeatable(sq, nh, nope, pe, pos0):
+    """Shapes with enough tiles per CTA run a static share per CTA and then
+    claim tail blocks dynamically: which CTA runs which block changes from call
+    to call, dO and dM must not (every block has its own dM partial slot)."""
+    O, dY, M = make_inputs(sq, nh, nope, pe, seed=sq + 5)
+    runs = [ir.invrope_postmix_bwd(dY, O, M, pos0, nope, pe) for _ in range(5)]
+    torch.cuda.synchronize()
+    for dO, dM in runs[1:]:
+        assert torch.equal(dO, runs[0][0])
+        assert torch.equal(dM, runs[0][1])
+    assert ir.invrope_take_device_fault() == 0
+    positions = np.arange(pos0, pos0 + sq, dtype=np.int64)
+    Y = ir.invrope_postmix_fwd(O, M, pos0, nope, pe)
+    compare_all_rows(O, dY, M, Y, runs[0][0], positions, nope, pe, 1e4)
+    dM_ref = oracle.postmix_bwd_dM(f64(dY), f64(O), positions, nope, pe, 1e4)
+    assert_dm_close(f64(runs[0][1]), dM_ref)
+
+
 def test_bwd_with_no_rows_zeroes_dM():
     O = torch.empty(0, 4, 64, dtype=torch.bfloat16, device="cuda")
     M = torch.eye(4, device="cuda")

@@ -134,26 +134,33 @@ def test_graph_replay_beside_many_eager_launches():
     assert ir.invrope_take_device_fault() == 0
 
 
-@pytest.mark.parametrize("which", ["fwd", "remap"])
+@pytest.mark.parametrize("which", ["fwd", "bwd", "remap"])
 def test_busy_slot_is_reported_not_shared(which):
     """The next launch's counter slot is marked as held by a launch tag that no
     launch has (a host-side write through the test hook): that launch must
     claim nothing from it and record the busy-slot code. Taking the fault frees
-    every slot, and the next call gives the bits of a plain call again."""
+    every slot, and the next call gives the bits of a plain call again. The
+    backward takes a slot (from the forward's slots) when it hands out tail
+    blocks, as at 4096 positions of 64 heads."""
     case = _case(43)
     O, dY, M, idx = case
     _, _, nope, pe = SHAPE
+    Ob, dYb, Mb = make_inputs(4096, 64, 448, 64, seed=44)
 
     def call():
         if which == "fwd":
             return ir.invrope_postmix_fwd(O, M, 7, nope, pe)
+        if which == "bwd":
+            return torch.cat([t.flatten().view(torch.int8) for t in
+                              ir.invrope_postmix_bwd(dYb, Ob, Mb, 16384, 448, 64)])
         return ir.kv_idx_local_to_global(idx, 512, 4096)
 
     ref = call()
     assert ir.invrope_take_device_fault() == 0
-    ir.invrope_debug_occupy_next_slot(which, (1 << 63) + 12345)
+    ir.invrope_debug_occupy_next_slot("remap" if which == "remap" else "fwd", (1 << 63) + 12345)
     call()  # finds its slot busy: output undefined
-    want = binding.INVROPE_FAULT_SCHED_BUSY_FWD if which == "fwd" else binding.INVROPE_FAULT_SCHED_BUSY_REMAP
+    want = {"fwd": binding.INVROPE_FAULT_SCHED_BUSY_FWD, "bwd": binding.INVROPE_FAULT_SCHED_BUSY_BWD,
+            "remap": binding.INVROPE_FAULT_SCHED_BUSY_REMAP}[which]
     assert ir.invrope_take_device_fault() == want
     for _ in range(3):
         assert torch.equal(call(), ref)
