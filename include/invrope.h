@@ -118,8 +118,11 @@ int invrope_postmix_fwd(const void* O, const float* M, void* Y,
 
 /*
  * Workspace bytes invrope_postmix_bwd needs on the CURRENT device for this
- * shape (one fp32 [nh, nh] partial of dM per thread block, so it depends on
- * the device's SM count). Returns 0 when the shape is invalid or unsupported.
+ * shape: fp32 [nh, nh] partials of dM, one per thread block and, for shapes
+ * whose thread blocks hand out the last ~10% of their tiles dynamically (the
+ * production split, nh = 64 with the pe block filling one 64-channel chunk),
+ * one per such tail block; so it depends on the device's SM count. At most
+ * 8 MiB for nh <= 64. Returns 0 when the shape is invalid or unsupported.
  */
 size_t invrope_postmix_bwd_workspace_bytes(int64_t sq, int nh, int nope, int pe);
 
@@ -139,10 +142,13 @@ size_t invrope_postmix_bwd_workspace_bytes(int64_t sq, int nh, int nope, int pe)
  *      contents on entry do not matter and are clobbered.
  * Outputs must not overlap each other, the inputs or the workspace.
  * Other arguments as in invrope_postmix_fwd. sq = 0 writes dM = 0.
- * dM is bitwise identical from run to run on the same device: partials are
- * formed per thread block in a fixed order and summed in block order (fp64
- * accumulation) without atomics. The rotated pe operand of dM is split into
- * bf16 hi + lo terms so that dM is not limited by bf16 rounding of X.
+ * dM is bitwise identical from run to run on the same device: each
+ * partial covers a fixed range of tiles accumulated in a fixed order
+ * (whichever thread block runs it), and the partials are summed in a fixed
+ * order (compensated fp32) without atomics. The rotated pe operand of dM is
+ * split into bf16 hi + lo terms so that dM is not limited by bf16 rounding of
+ * X. Shapes that hand out tail blocks take one work-counter slot (see the
+ * common contract) and may record INVROPE_FAULT_SCHED_BUSY_BWD.
  */
 int invrope_postmix_bwd(const void* dY, const void* O, const float* M,
                         void* dO, float* dM,

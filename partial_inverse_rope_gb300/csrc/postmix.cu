@@ -94,8 +94,12 @@ enum : unsigned { kBarFull = 1, kBarEmpty, kBarAccFull, kBarAccEmpty, kBarXFull,
 
 // WIDE (backward with one position per tile, nh > 64): 128-channel tiles, so
 // each head-mix MMA has N = 128 and a tile needs half as many of them.
-template <bool BWD, bool WIDE = false>
+// STK (backward, nh = 64, pe block = one whole chunk): the stacked head mix,
+// with A = [M^T_hi ; M^T_lo] in shared memory so that TMEM holds two D2
+// buffers (the drain of one segment overlaps the next segment's dM chains).
+template <bool BWD, bool WIDE = false, bool STK = false>
 struct KCfg {
+  static_assert(!STK || (BWD && !WIDE), "the stacked mix is a 64-channel backward");
   static constexpr int NC = (BWD && !WIDE) ? 64 : 128;   // channels per tile
   static constexpr int kChunks = NC / kChunkCols;
   static constexpr int kTensorTile = kChunks * kChunkBytes;
@@ -104,7 +108,9 @@ struct KCfg {
   static constexpr int kOutBufs = BWD ? 3 : 5;           // output ring of 64-channel chunks
   static constexpr int kOutInflight = kOutBufs - 2;      // TMA stores left reading smem
   static constexpr int kNumAcc = BWD ? (WIDE ? 2 : 4) : 3;
-  // TMEM columns: accumulators, then dM (bwd), then A hi (64) and A lo (64)
+  static constexpr int kNumD2 = STK ? 2 : 1;
+  // TMEM columns: accumulators, then dM (bwd: one or two 128-column buffers),
+  // then (all but STK) A hi (64) and A lo (64)
   static constexpr int kD2Col = kNumAcc * NC;
   static constexpr int kACol = 384;
   static constexpr int kTmemCols = 512;
@@ -118,21 +124,25 @@ struct KCfg {
   static constexpr int kXloBytes = BWD ? kChunks * kChunkBytes : 0;
   // bwd, stacked mix: fp32 exchange rows between the epilogue warp pairs (64 x 256 B)
   static constexpr int kOffXch = kOffXlo + kXloBytes;
-  static constexpr int kXchBytes = (BWD && !WIDE) ? 64 * 256 : 0;
-  static constexpr int kTabBytes = kPosPerTileMax * kMaxHalf * 8;
-  static constexpr int kOffTabEpi = kOffXch + kXchBytes;
+  static constexpr int kXchBytes = STK ? 64 * 256 : 0;
+  // STK: A = [M^T_hi ; M^T_lo], 128 rows of 64 bf16, 128-byte-swizzled K-major
+  static constexpr int kOffA = kOffXch + kXchBytes;
+  static constexpr int kABytes = STK ? kChunkBytes : 0;
+  // rotation tables: positions per tile x 32 pairs (STK: 2 positions)
+  static constexpr int kTabBytes = (STK ? 2 : kPosPerTileMax) * kMaxHalf * 8;
+  static constexpr int kOffTabEpi = kOffA + kABytes;
   static constexpr int kOffTabXf = kOffTabEpi + kTabBytes;
   static constexpr int kOffFreq = kOffTabXf + (BWD ? kTabBytes : 0);
   static constexpr int kOffBars = kOffFreq + kMaxHalf * 8;
-  // + backward segment ring (4 full, 4 empty) and the D2 hand-back
-  static constexpr int kNumBars = 2 * kStages + 2 * kOutBufs + 2 * kNumAcc + 6 + (BWD ? 9 : 0);
+  // + backward: segment ring (4 full, 4 empty), D2 hand-back, second D2 pair
+  static constexpr int kNumBars = 2 * kStages + 2 * kOutBufs + 2 * kNumAcc + 6 + (BWD ? 11 : 0);
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   // tmem base, abort flag, wait slots, tile ids (192 B), backward segment ring
   // and its broadcast slots (128 B)
   static constexpr int kSmemBytes = kOffMisc + 192 + (BWD ? 128 : 0);
   static constexpr int kSmemAlloc = kSmemBytes + 1024;   // slack to align the base
   static_assert(kSmemAlloc <= 232448, "shared memory budget");
-  static_assert(kNumAcc * NC + (BWD ? 128 : 0) <= kACol, "TMEM budget");
+  static_assert(kNumAcc * NC + (BWD ? kNumD2 * 128 : 0) <= (STK ? kTmemCols : kACol), "TMEM budget");
   static_assert(kStages * kStageBytes >= 128 * 129 * 4, "dM partial reduction reuses the input ring");
   static_assert(kOutInflight >= 1, "at least one store in flight");
   static_assert(kOffFreq - kOffOut >= 128 * 128 * 4, "M is copied into the output ring and the buffers after it");
@@ -170,10 +180,11 @@ struct PostmixParams {
   double log2_theta;   // rotary frequencies beyond the first 32 pairs are formed on the device
   // Backward schedule: CTA c first runs tiles [n_static c / G, n_static (c+1) / G)
   // into dM partial slot c; the tiles from n_static on form n_tail fixed blocks
-  // (tail_na of tail_ba tiles, then blocks of tail_bb tiles), claimed one at a
-  // time from the launch's counter slot, block b into partial slot G + b.
+  // (tail_na of tail_ba tiles, tail_nb of tail_bb tiles, then blocks of tail_bc
+  // tiles), claimed one at a time from the launch's counter slot, block b into
+  // partial slot G + b.
   int64_t n_static;
-  int n_tail, tail_na, tail_ba, tail_bb;
+  int n_tail, tail_na, tail_ba, tail_nb, tail_bb, tail_bc;
 };
 
 // kind 0: a tile of the regular tiling (channels c0 + 64 k, TMA-stored);
@@ -403,10 +414,10 @@ struct MixLine {
   }
 };
 
-template <bool BWD, bool WIDE = false>
-__global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
+template <bool BWD, bool WIDE = false, bool STK = false>
+__global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
     postmix_kernel(const __grid_constant__ PostmixParams p) {
-  using C = KCfg<BWD, WIDE>;
+  using C = KCfg<BWD, WIDE, STK>;
   // the general tiling's pair blocks occur in the forward and the 128-channel backward only
   constexpr bool kGen = !BWD || WIDE;
   extern __shared__ uint8_t smem_raw[];
@@ -437,6 +448,9 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
   auto bar_seg_full = [&](int k) { return bar_x_full + 48 + 8u * k; };
   auto bar_seg_empty = [&](int k) { return bar_x_full + 80 + 8u * k; };
   const uint32_t bar_d2_empty = bar_x_full + 112;
+  // D2 buffer b: full (the segment's last dM MMA completed) and empty (drained)
+  auto bar_d2f = [&](int b) { return b ? bar_x_full + 120 : bar_d2; };
+  auto bar_d2e = [&](int b) { return b ? bar_x_full + 128 : bar_d2_empty; };
   auto stage_addr = [&](int s) { return base + C::kOffStage + static_cast<uint32_t>(s) * C::kStageBytes; };
   auto out_addr = [&](int b) { return base + C::kOffOut + static_cast<uint32_t>(b) * kChunkBytes; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
@@ -463,7 +477,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
   const int half = p.pe >> 1;
   // Accumulator ring: NA accumulators of NC columns, or 2 of 128 columns for the
   // stacked backward mix (the same 256 TMEM columns).
-  const bool stk = BWD && p.stacked != 0;
+  constexpr bool stk = STK;
   static_assert(!BWD || NA == 4 || NA == 2, "the backward ring is indexed with shifts");
   const uint32_t na_sh = (stk || NA == 2) ? 1u : 2u;
   const uint32_t acc_cols = stk ? 128u : static_cast<uint32_t>(C::NC);
@@ -500,7 +514,10 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
         ptx::mbar_init(bar_seg_full(k), 1);
         ptx::mbar_init(bar_seg_empty(k), 4);  // MMA thread, epilogue, store warp, transform warps
       }
-      ptx::mbar_init(bar_d2_empty, 128);
+      for (int b = 0; b < C::kNumD2; ++b) {
+        if (b) ptx::mbar_init(bar_d2f(b), 1);
+        ptx::mbar_init(bar_d2e(b), 128);
+      }
     }
     *abort_flag = 0;
     // take the launch's counter slot; if another launch still holds it, claim
@@ -555,10 +572,19 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
   // static share (dM partial slot blockIdx.x), then the tail blocks this CTA
   // claimed (slot G + b). The producer publishes them through a 4-entry ring.
   auto tail_block = [&](uint32_t b, int64_t& t0, int64_t& t1) {
-    const uint32_t na = static_cast<uint32_t>(p.tail_na);
-    t0 = b < na ? p.n_static + static_cast<int64_t>(b) * p.tail_ba
-                : p.n_static + static_cast<int64_t>(na) * p.tail_ba + static_cast<int64_t>(b - na) * p.tail_bb;
-    t1 = t0 + (b < na ? p.tail_ba : p.tail_bb);
+    const uint32_t na = static_cast<uint32_t>(p.tail_na), nab = na + static_cast<uint32_t>(p.tail_nb);
+    const int64_t a_end = p.n_static + static_cast<int64_t>(na) * p.tail_ba;
+    const int64_t b_end = a_end + static_cast<int64_t>(p.tail_nb) * p.tail_bb;
+    if (b < na) {
+      t0 = p.n_static + static_cast<int64_t>(b) * p.tail_ba;
+      t1 = t0 + p.tail_ba;
+    } else if (b < nab) {
+      t0 = a_end + static_cast<int64_t>(b - na) * p.tail_bb;
+      t1 = t0 + p.tail_bb;
+    } else {
+      t0 = b_end + static_cast<int64_t>(b - nab) * p.tail_bc;
+      t1 = t0 + p.tail_bc;
+    }
     if (t1 > p.n_tiles) t1 = p.n_tiles;
   };
   auto seg_publish = [&](uint32_t k, int64_t t0, int64_t t1, int slot) -> bool {
@@ -623,8 +649,9 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
         msm = p.m_bulk != 0;
         if (msm) wait_bar(bar_m, 0, abort_flag, (kRoleEpilogue << 8) | kBarM);
       }
-      if (BWD && p.stacked) {
-        // stacked A: lane m < 64 holds M^T_hi row m, lane 64 + h holds M^T_lo row h
+      if constexpr (STK) {
+        // stacked A in shared memory (128-byte-swizzled K-major rows, K = the
+        // 64 heads): row m < 64 is M^T_hi row m, row 64 + h is M^T_lo row h
         const MixLine col(p, m & 63, false);
         float v[64];
 #pragma unroll
@@ -635,7 +662,10 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
           const uint32_t hw = ptx::pack_bf16x2(v[2 * q], v[2 * q + 1]);
           w[q] = m < 64 ? hw : ptx::pack_bf16x2(v[2 * q] - ptx::bf16_lo_f32(hw), v[2 * q + 1] - ptx::bf16_hi_f32(hw));
         }
-        ptx::tmem_st_x32(row_addr, w);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          ptx::st_shared_v4(swz_unit_addr(base + C::kOffA, m, 8 * u), w[4 * u], w[4 * u + 1], w[4 * u + 2],
+                            w[4 * u + 3]);
       } else {
         // A = blockdiag_P(M) (forward) or blockdiag_P(M^T) (backward): row m
         // (position m / nh, head m % nh) is nonzero on columns [pb, pb + nh) only
@@ -706,30 +736,42 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
       // from the launch's counter, one claim ahead. Backward: the static share,
       // then tail blocks claimed one segment ahead, each segment published to
       // the other roles before its first tile is loaded.
+      // The next tail block is claimed a few tiles before the current segment
+      // ends, so that the claims come in the order in which CTAs run out of
+      // work (the claim's latency hides behind those tiles' loads).
+      constexpr int64_t kClaimAhead = 3;
       int64_t t_next = BWD ? t_begin : static_cast<int64_t>(blockIdx.x);
       int64_t seg_end = t_end;
       uint32_t seg_k = 0;
       uint32_t claim = 0xffffffffu;
+      bool claimed = false;
       bool run = true;
-      if constexpr (BWD) {
-        run = !*abort_flag && seg_publish(0, t_begin, t_end, static_cast<int>(blockIdx.x));
-        if (run && p.n_tail > 0) claim = atomicAdd(&p.sched->next, 1u);
-      }
+      if constexpr (BWD) run = !*abort_flag && seg_publish(0, t_begin, t_end, static_cast<int>(blockIdx.x));
       for (uint32_t i = 0; run; ++i) {
         const int st = static_cast<int>(i % S);
         const uint32_t ph = (i / S) & 1u;
-        if (BWD && t_next >= seg_end) {
-          ++seg_k;
-          if (claim >= static_cast<uint32_t>(p.n_tail)) {
-            seg_publish(seg_k, -1, -1, -1);
-            break;
+        if constexpr (BWD) {
+          if (!claimed && p.n_tail > 0 && seg_end - t_next <= kClaimAhead) {
+            claim = atomicAdd(&p.sched->next, 1u);
+            claimed = true;
           }
-          int64_t a0 = 0, a1 = 0;
-          tail_block(claim, a0, a1);
-          if (!seg_publish(seg_k, a0, a1, static_cast<int>(G + claim))) break;
-          t_next = a0;
-          seg_end = a1;
-          claim = atomicAdd(&p.sched->next, 1u);
+          if (t_next >= seg_end) {
+            ++seg_k;
+            if (!claimed || claim >= static_cast<uint32_t>(p.n_tail)) {
+              seg_publish(seg_k, -1, -1, -1);
+              break;
+            }
+            int64_t a0 = 0, a1 = 0;
+            tail_block(claim, a0, a1);
+            if (!seg_publish(seg_k, a0, a1, static_cast<int>(G + claim))) break;
+            t_next = a0;
+            seg_end = a1;
+            claimed = false;
+            if (seg_end - t_next <= kClaimAhead) {
+              claim = atomicAdd(&p.sched->next, 1u);
+              claimed = true;
+            }
+          }
         }
         if (*abort_flag) break;
         if (!wait_bar(bar_empty(st), ph ^ 1u, abort_flag, (kRoleProducer << 8) | kBarEmpty)) break;
@@ -768,29 +810,34 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t nks = static_cast<uint32_t>((p.R + 15) / 16);
-      uint32_t d2_started = 0;
+      uint32_t d2_started = 0;  // bit b: D2 buffer b has taken a dM MMA in its segment
       int npe = 0;
-      // D2 of a new segment may start only once the drain has read the last one out
-      bool d2_wait = false;
+      // A segment's first dM MMA into D2 buffer d2_wait_b waits until the drain
+      // has read out the segment that used the buffer before (phase d2_par).
+      int d2_wait_b = -1;
       uint32_t d2_par = 0;
-      // D2 += dY_tile * X_tile^T (both K-major, K = channels), plus dY_pe * X_lo^T on a pe tile
-      auto dm_chain = [&](int st, const Tile& x) -> bool {
-        if (d2_wait) {
-          if (!wait_bar(bar_d2_empty, d2_par, abort_flag, (kRoleMma << 8) | kBarD2Empty)) return false;
+      int cur_b = 0;   // D2 buffer of the segment being issued
+      int owe_b = -1;  // STK: buffer whose segment is complete once the pending pe tile's chain is out
+      // D2[b] += dY_tile * X_tile^T (both K-major, K = channels), plus dY_pe * X_lo^T on a pe tile
+      auto dm_chain = [&](int st, const Tile& x, int b) -> bool {
+        if (b == d2_wait_b) {
+          if (!wait_bar(bar_d2e(b), d2_par, abort_flag, (kRoleMma << 8) | kBarD2Empty)) return false;
           ptx::tc_fence_after();
-          d2_wait = false;
+          d2_wait_b = -1;
         }
         const uint32_t sa = stage_addr(st);
-        const uint32_t d2 = tmem_base + C::kD2Col;
+        const uint32_t d2 = tmem_base + C::kD2Col + static_cast<uint32_t>(b) * 128u;
+        uint32_t started = (d2_started >> b) & 1u;
         const uint32_t idesc_dm = ptx::idesc_bf16_f32(128, 128, false, false);
         const uint32_t xa = sa + C::kTensorTile;
         for (int k = 0; k < x.nch; ++k)
           for (uint32_t kk = 0; kk < 4; ++kk) {
             const uint64_t ad = ptx::smem_desc_sw128(sa + k * kChunkBytes + kk * 32, 16, 1024);
             const uint64_t bd = ptx::smem_desc_sw128(xa + k * kChunkBytes + kk * 32, 16, 1024);
-            ptx::tc_mma_ss(d2, ad, bd, idesc_dm, d2_started);
-            d2_started = 1;
+            ptx::tc_mma_ss(d2, ad, bd, idesc_dm, started);
+            started = 1;
           }
+        d2_started |= 1u << b;
         if (x.has_pe) {
           // the lo terms of X: one box (the pe box of a regular tile) or both
           // boxes of a general pair block, X_lo box b pairing with dY box kpe + b
@@ -806,18 +853,22 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
         }
         return true;
       };
-      // the pe tile whose dM chain is still to be issued (stage, tile)
-      int pend_st = -1;
+      // the pe tile whose dM chain is still to be issued (stage, tile, D2 buffer)
+      int pend_st = -1, pend_b = 0;
       Tile pend_x{};
       auto flush_pending = [&]() {
         if (!wait_bar(bar_x_full, static_cast<uint32_t>(npe & 1), abort_flag, (kRoleMma << 8) | kBarXFull))
           return false;
         ptx::tc_fence_after();
-        if (!dm_chain(pend_st, pend_x)) return false;
+        if (!dm_chain(pend_st, pend_x, pend_b)) return false;
         ptx::tc_commit(bar_empty(pend_st));
         ptx::tc_commit(bar_x_empty);
         ++npe;
         pend_st = -1;
+        if (STK && owe_b >= 0) {  // that tile ended its segment: D2[owe_b] goes to the drain
+          ptx::tc_commit(bar_d2f(owe_b));
+          owe_b = -1;
+        }
         return true;
       };
       // Backward: an outer loop over the segments, the per-tile loop within
@@ -831,6 +882,15 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
           if (!seg_read(seg_k, s_t, s_t1, s_slot, (kRoleMma << 8) | kBarSeg)) break;
           ++seg_k;
           if (s_t < 0) break;
+          // segment k = seg_k - 1 accumulates into D2 buffer k mod kNumD2,
+          // after the drain of segment k - kNumD2 that used it before
+          const uint32_t k = seg_k - 1;
+          cur_b = STK ? static_cast<int>(k & 1u) : 0;
+          d2_started &= ~(1u << cur_b);
+          if (k >= static_cast<uint32_t>(C::kNumD2)) {
+            d2_wait_b = cur_b;
+            d2_par = ((k / C::kNumD2) - 1u) & 1u;
+          }
         }
         bool seg_done = false;
       for (;; ++i) {
@@ -871,13 +931,15 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
         const uint32_t sa = stage_addr(st);
         // head mix: D[acc] = A_hi * B + A_lo * B, A in TMEM, B = the tile (MN-major, K = rows)
         const uint32_t d_acc = tmem_base + static_cast<uint32_t>(acc) * acc_cols;
-        if (stk) {
+        if constexpr (STK) {
           // stacked: D[128 x 128] = [M^T_hi ; M^T_lo] * [tile rows 0-63 | tile rows 64-127],
-          // K = the 64 heads of a position; N block 1 sits 64 rows (8 KB) below N block 0
+          // K = the 64 heads of a position (A K-major in shared memory); N block
+          // 1 sits 64 rows (8 KB) below N block 0
           const uint32_t idesc_stk = ptx::idesc_bf16_f32(128, 128, false, true);
           for (uint32_t ks = 0; ks < 4; ++ks) {
+            const uint64_t ad = ptx::smem_desc_sw128(base + C::kOffA + ks * 32, 16, 1024);
             const uint64_t bd = ptx::smem_desc_sw128(sa + ks * 2048, 64 * 128, 1024);
-            ptx::tc_mma_ts(d_acc, tmem_base + C::kACol + ks * 8, bd, idesc_stk, ks != 0);
+            ptx::tc_mma_ss(d_acc, ad, bd, idesc_stk, ks != 0);
           }
         } else {
           const uint32_t idesc_mix = ptx::idesc_bf16_f32(128, 64u * x.nch, false, true);
@@ -899,25 +961,35 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
         // the input ring keep moving while X is formed. The issue order is fixed
         // by the tile sequence alone, so D2 (and dM) stay reproducible.
         if (!x.has_pe) {
-          if (!dm_chain(st, x)) break;
+          if (!dm_chain(st, x, cur_b)) break;
           ptx::tc_commit(bar_empty(st));
         }
         if (pend_st >= 0 && !flush_pending()) break;
         if (x.has_pe && !handoff_early) ptx::mbar_arrive(bar_x_go);
         if (x.has_pe) {
           pend_st = st;
+          pend_b = cur_b;
           pend_x = x;
         }
       }
         if (!seg_done) break;  // forward: the end of the tile stream; else a wait gave up
-        // The segment is issued: its last pe tile's dM chain goes out, then D2
-        // is handed to the drain (transform warps) once every MMA so far
-        // completes; the next segment's D2 starts from zero.
-        if (pend_st >= 0 && !flush_pending()) break;
-        ptx::tc_commit(bar_d2);
-        d2_wait = true;
-        d2_par = (seg_k - 1) & 1u;
-        d2_started = 0;
+        // The segment is issued. D2 goes to the drain (transform warps) once
+        // every MMA so far completes, after the segment's last dM chain: with
+        // one D2 buffer the pending pe tile's chain goes out now; with two it
+        // keeps its usual place one tile later (in the next segment) and the
+        // hand-over follows it.
+        if constexpr (STK) {
+          if (pend_st >= 0)
+            owe_b = cur_b;
+          else
+            ptx::tc_commit(bar_d2f(cur_b));
+        } else {
+          if (pend_st >= 0 && !flush_pending()) break;
+          ptx::tc_commit(bar_d2);
+        }
+      }
+      if constexpr (STK) {
+        if (pend_st >= 0) flush_pending();  // the last segment ended with a pe tile
       }
       // every MMA issued must complete before TMEM is freed, abort or not
       ptx::tc_commit(bar_done);
@@ -1341,18 +1413,64 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
       // [pl nh, pl nh + nh). The D2 columns are handed back (bar_d2_empty) as
       // soon as they are read.
       auto drain_d2 = [&](uint32_t k, int slot) -> bool {
-        if (!group_wait(bar_d2, k & 1u, abort_flag, (kRoleTransform << 8) | kBarD2, xr == 0, slot_d2, 2))
+        // segment k used D2 buffer k mod kNumD2
+        const int b = static_cast<int>(k % C::kNumD2);
+        if (!group_wait(bar_d2f(b), (k / C::kNumD2) & 1u, abort_flag, (kRoleTransform << 8) | kBarD2, xr == 0,
+                        slot_d2, 2))
           return false;
         ptx::tc_fence_after();
         const uint32_t q4 = static_cast<uint32_t>(warp & 3);
         const int r = static_cast<int>(q4 * 32u) + lane;  // this thread's TMEM lane: D2 row r
-        const uint32_t taddr = tmem_base + ((q4 * 32u) << 16) + C::kD2Col;
+        const uint32_t taddr = tmem_base + ((q4 * 32u) << 16) + C::kD2Col + static_cast<uint32_t>(b) * 128u;
         const bool rok = r < p.R;
         const int nh = p.nh;
         const int pl = rok ? r / nh : 0, g = r - pl * nh;
         const int lo = pl * nh, hi = lo + nh;
         float* dst = p.ws + static_cast<int64_t>(slot) * nh * nh;
-        if (p.P == 1) {
+        if constexpr (STK) {
+          // nh = 64, two positions: row r's block row is columns [64 pl, 64 pl + 64)
+          // (pl is uniform per warp). Position 1's rows park theirs in X_lo
+          // (16-byte unit u of row g at u ^ (g & 15)), position 0's rows add
+          // them and write partial row g. The other D2 buffer takes the next
+          // segment meanwhile, so nothing waits for this hand-back.
+          float4* xch = reinterpret_cast<float4*>(gbase + C::kOffXlo);
+          if (pl == 1) {
+            for (int h2 = 0; h2 < 2; ++h2) {
+              uint32_t v[32];
+              ptx::tmem_ld_x32(taddr + 64u + 32u * h2, v);
+              ptx::tmem_ld_wait(v);
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int uu = 8 * h2 + u;
+                xch[g * 16 + (uu ^ (g & 15))] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                                            __uint_as_float(v[4 * u + 2]),
+                                                            __uint_as_float(v[4 * u + 3]));
+              }
+            }
+          }
+          ptx::named_bar_sync(2, 128);
+          if (pl == 0) {
+            float4* drow = reinterpret_cast<float4*>(dst + static_cast<int64_t>(g) * 64);
+            for (int h2 = 0; h2 < 2; ++h2) {
+              uint32_t v[32];
+              ptx::tmem_ld_x32(taddr + 32u * h2, v);
+              ptx::tmem_ld_wait(v);
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int uu = 8 * h2 + u;
+                const float4 o = xch[g * 16 + (uu ^ (g & 15))];
+                drow[uu] = make_float4(__uint_as_float(v[4 * u]) + o.x, __uint_as_float(v[4 * u + 1]) + o.y,
+                                       __uint_as_float(v[4 * u + 2]) + o.z, __uint_as_float(v[4 * u + 3]) + o.w);
+              }
+            }
+          }
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar_d2e(b));
+          ptx::named_bar_sync(2, 128);  // every row has read X_lo
+          for (uint32_t o = static_cast<uint32_t>(xr) * 16u; o < static_cast<uint32_t>(C::kXloBytes); o += 128u * 16u)
+            ptx::st_shared_v4(base + C::kOffXlo + o, 0u, 0u, 0u, 0u);
+          ptx::fence_proxy_async_smem();
+        } else if (p.P == 1) {
           // one position per tile: D2 row r is partial row r
           for (int j0 = 0; j0 < nh; j0 += 32) {
             uint32_t v[32];
@@ -1373,7 +1491,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
             }
           }
           ptx::tc_fence_before();
-          ptx::mbar_arrive(bar_d2_empty);
+          ptx::mbar_arrive(bar_d2e(b));
         } else if (p.P == 2) {
           // Position 1's rows park theirs in X_lo (free now: the segment's last
           // dM chain has completed), row g at g * 64 with column c at c ^ (g & 31)
@@ -1408,7 +1526,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
             }
           }
           ptx::tc_fence_before();
-          ptx::mbar_arrive(bar_d2_empty);
+          ptx::mbar_arrive(bar_d2e(b));
           ptx::named_bar_sync(2, 128);  // every row has read X_lo
           // X_lo back to zero: the pe transform writes only its pe columns
           for (uint32_t o = static_cast<uint32_t>(xr) * 16u; o < static_cast<uint32_t>(C::kXloBytes); o += 128u * 16u)
@@ -1434,7 +1552,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE>::kThreads, 1)
             }
           }
           ptx::tc_fence_before();
-          ptx::mbar_arrive(bar_d2_empty);
+          ptx::mbar_arrive(bar_d2e(b));
           ptx::named_bar_sync(2, 128);
           const int nn = nh * nh;
           // consecutive threads take consecutive h: coalesced partial rows
@@ -1772,7 +1890,8 @@ struct Shape {
   int64_t n_tiles;
   bool gen;   // general tiling: the pe block does not lie inside one 64-channel box
   bool wide;  // backward: 128-channel tiles (one position per tile, or the general tiling)
-  bool tail_ok = false;  // backward: the kernel can hand out tail blocks
+  bool stacked = false;  // backward, nh = 64, pe block = one whole chunk: the stacked kernel
+  bool tail_ok = false;  // backward: the kernel can hand out tail blocks (the stacked one)
 };
 
 // Validate a postmix shape and lay out its tiles (forward, or backward if bwd).
@@ -1785,6 +1904,8 @@ int check_shape(int64_t sq, int nh, int nope, int pe, bool bwd, Shape* s) {
   if (sq * nh >= (int64_t(1) << 31)) return INVROPE_ERR_UNSUPPORTED;
   s->gen = nope / kChunkCols != (d - 1) / kChunkCols;
   s->wide = bwd && (s->gen || nh > 64);
+  s->stacked = bwd && !s->wide && nh == 64 && pe == kChunkCols && nope % kChunkCols == 0;
+  s->tail_ok = s->stacked;
   const int nc = (!bwd || s->wide) ? 2 * kChunkCols : kChunkCols;
   s->P = 128 / nh < kPosPerTileMax ? 128 / nh : kPosPerTileMax;
   s->R = s->P * nh;
@@ -1823,16 +1944,16 @@ bool make_maps(PostmixParams* p, const Shape& s, const void* in0, const void* in
   return true;
 }
 
-template <bool BWD, bool WIDE = false>
+template <bool BWD, bool WIDE = false, bool STK = false>
 int ensure_smem_attr(int device) {
   static std::mutex mu;
   static bool done[64] = {};
   std::lock_guard<std::mutex> lock(mu);
   if (device < 0 || device >= 64) return INVROPE_ERR_DEVICE;
   if (!done[device]) {
-    const cudaError_t err = cudaFuncSetAttribute(postmix_kernel<BWD, WIDE>,
+    const cudaError_t err = cudaFuncSetAttribute(postmix_kernel<BWD, WIDE, STK>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 KCfg<BWD, WIDE>::kSmemAlloc);
+                                                 KCfg<BWD, WIDE, STK>::kSmemAlloc);
     if (err != cudaSuccess) return cuda_fail(err);
     done[device] = true;
   }
@@ -1868,7 +1989,7 @@ static int64_t bwd_grid(const Shape& s, int sms) { return s.n_tiles < sms ? s.n_
 // slots stay within 8 MiB (or twice the static slots).
 struct TailPlan {
   int64_t n_static = 0;
-  int n_tail = 0, na = 0, ba = 0, bb = 0;
+  int n_tail = 0, na = 0, ba = 0, nb = 0, bb = 0, bc = 0;
 };
 
 static TailPlan bwd_tail_plan(const Shape& s, int64_t grid, int nh) {
@@ -1881,15 +2002,19 @@ static TailPlan bwd_tail_plan(const Shape& s, int64_t grid, int nh) {
   const int64_t budget = std::max<int64_t>(int64_t(8) << 20, 2 * grid * slot_bytes);
   const int64_t max_tail = budget / slot_bytes - grid;
   if (max_tail < grid) return t;
-  // level A: one block per CTA of ~1/12 of a share; level B: small blocks of
-  // ~1/48 of a share for the end
-  t.ba = static_cast<int>(std::max<int64_t>(4, per / 12));
-  t.bb = static_cast<int>(std::max<int64_t>(2, per / 48));
-  t.na = static_cast<int>(grid);
-  const int64_t nb = std::min<int64_t>(max_tail - grid, grid * 3 / 2);
-  const int64_t tail = static_cast<int64_t>(t.na) * t.ba + nb * t.bb;
+  // Blocks shrink as the tail runs out (~11% of the tiles in all): half as
+  // many as CTAs of ~1/11 of a share (the CTAs that finish their share
+  // first), one per CTA of ~1/22, and the rest of the slots in blocks of
+  // ~1/54 of a share for the end.
+  t.ba = static_cast<int>(std::max<int64_t>(4, per / 11));
+  t.bb = static_cast<int>(std::max<int64_t>(2, per / 22));
+  t.bc = static_cast<int>(std::max<int64_t>(1, per / 54));
+  t.na = static_cast<int>(grid / 2);
+  t.nb = static_cast<int>(std::min<int64_t>(grid, max_tail - t.na));
+  const int64_t nc = std::max<int64_t>(0, std::min<int64_t>(max_tail - t.na - t.nb, grid));
+  const int64_t tail = static_cast<int64_t>(t.na) * t.ba + static_cast<int64_t>(t.nb) * t.bb + nc * t.bc;
   t.n_static = s.n_tiles - tail;
-  t.n_tail = static_cast<int>(t.na + nb);
+  t.n_tail = static_cast<int>(t.na + t.nb + nc);
   return t;
 }
 
@@ -2014,7 +2139,9 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (grid > 0) {
     const bool wide = s.wide;
-    if ((st = wide ? ensure_smem_attr<true, true>(dev.device) : ensure_smem_attr<true>(dev.device)) != INVROPE_OK)
+    if ((st = wide        ? ensure_smem_attr<true, true>(dev.device)
+              : s.stacked ? ensure_smem_attr<true, false, true>(dev.device)
+                          : ensure_smem_attr<true>(dev.device)) != INVROPE_OK)
       return st;
     PostmixParams p;
     std::memset(&p, 0, sizeof(p));
@@ -2035,7 +2162,7 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
     p.R = s.R;
     p.n_ct = s.n_ct;
     // stacked head mix: two positions of 64 heads per tile, pe block = one chunk
-    p.stacked = (!wide && nh == 64 && pe == kChunkCols && nope % kChunkCols == 0) ? 1 : 0;
+    p.stacked = s.stacked ? 1 : 0;
     p.pos = positions;
     p.gs = gs;
     p.gen = s.gen ? 1 : 0;
@@ -2047,7 +2174,9 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
     p.n_tail = tail.n_tail;
     p.tail_na = tail.na;
     p.tail_ba = tail.ba;
+    p.tail_nb = tail.nb;
     p.tail_bb = tail.bb;
+    p.tail_bc = tail.bc;
     p.sched = nullptr;
     if (tail.n_tail > 0 &&
         (st = slot_take(g_sched_ring, &g_sched, dev.device, cs, &p.sched)) != INVROPE_OK)
@@ -2056,6 +2185,9 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
     if (wide)
       postmix_kernel<true, true>
           <<<static_cast<unsigned>(grid), KCfg<true, true>::kThreads, KCfg<true, true>::kSmemAlloc, cs>>>(p);
+    else if (s.stacked)
+      postmix_kernel<true, false, true><<<static_cast<unsigned>(grid), KCfg<true, false, true>::kThreads,
+                                          KCfg<true, false, true>::kSmemAlloc, cs>>>(p);
     else
       postmix_kernel<true><<<static_cast<unsigned>(grid), KCfg<true>::kThreads, KCfg<true>::kSmemAlloc, cs>>>(p);
     if ((st = check_launch()) != INVROPE_OK) return st;
