@@ -1886,10 +1886,10 @@ void fill_freq(uint64_t* F, int pe, double theta) {
 }
 
 struct Shape {
-  int P, R, n_ct, n_nope_ct;
-  int64_t n_tiles;
-  bool gen;   // general tiling: the pe block does not lie inside one 64-channel box
-  bool wide;  // backward: 128-channel tiles (one position per tile, or the general tiling)
+  int P = 0, R = 0, n_ct = 0, n_nope_ct = 0;
+  int64_t n_tiles = 0;
+  bool gen = false;   // general tiling: the pe block does not lie inside one 64-channel box
+  bool wide = false;  // backward: 128-channel tiles (one position per tile, or the general tiling)
   bool stacked = false;  // backward, nh = 64, pe block = one whole chunk: the stacked kernel
   bool tail_ok = false;  // backward: the kernel can hand out tail blocks (the stacked one)
 };
@@ -1905,10 +1905,13 @@ int check_shape(int64_t sq, int nh, int nope, int pe, bool bwd, Shape* s) {
   s->gen = nope / kChunkCols != (d - 1) / kChunkCols;
   s->wide = bwd && (s->gen || nh > 64);
   s->stacked = bwd && !s->wide && nh == 64 && pe == kChunkCols && nope % kChunkCols == 0;
-  s->tail_ok = s->stacked;
   const int nc = (!bwd || s->wide) ? 2 * kChunkCols : kChunkCols;
   s->P = 128 / nh < kPosPerTileMax ? 128 / nh : kPosPerTileMax;
   s->R = s->P * nh;
+  // tail blocks: the stacked kernel, whose double-buffered D2 makes segment
+  // changes free (the 128-channel kernel's CTAs finish within ~25 us of each
+  // other under the static split, and a single D2's hand-back costs more)
+  s->tail_ok = s->stacked;
   if (!s->gen) {
     s->n_nope_ct = 0;
     s->n_ct = static_cast<int>((d + nc - 1) / nc);
@@ -1997,7 +2000,7 @@ static TailPlan bwd_tail_plan(const Shape& s, int64_t grid, int nh) {
   t.n_static = s.n_tiles;
   const int64_t per = s.n_tiles / (grid > 0 ? grid : 1);
   const int64_t slot_bytes = static_cast<int64_t>(nh) * nh * 4;
-  if (s.P > 2 || per < 96 || slot_bytes > 16 * 1024) return t;
+  if (s.P > 2 || per < 96) return t;
   if (!s.tail_ok) return t;
   const int64_t budget = std::max<int64_t>(int64_t(8) << 20, 2 * grid * slot_bytes);
   const int64_t max_tail = budget / slot_bytes - grid;
