@@ -525,8 +525,9 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
     if (use_sched && !sched_mine)
       record_fault(BWD ? INVROPE_FAULT_SCHED_BUSY_BWD : INVROPE_FAULT_SCHED_BUSY_FWD, abort_flag);
     ptx::fence_mbar_init();
-    // forward: M goes out first, ahead of every tile load; the A build waits on it
-    if (!BWD && p.m_bulk) {
+    // M goes out first, ahead of every tile load (into the output ring, idle
+    // until the first tile is mixed); the A build waits on it
+    if (p.m_bulk) {
       const uint32_t mbytes = static_cast<uint32_t>(p.nh * p.gs * 4);
       ptx::mbar_arrive_expect_tx(bar_m, mbytes);
       ptx::bulk_load(base + C::kOffOut, p.M, mbytes, bar_m);
@@ -544,7 +545,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
     // before anything warp-collective follows
     const char* mb = reinterpret_cast<const char*>(p.M);
     const int mbytes = p.nh * p.gs * 4;
-    if (BWD || !p.m_bulk)
+    if (!p.m_bulk)
       for (int o = lane * 128; o < mbytes; o += 32 * 128) ptx::prefetch_l2(mb + o);
     __syncwarp();
   }
@@ -641,21 +642,19 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
       const uint32_t quad = static_cast<uint32_t>(warp & 3);
       const int m = static_cast<int>(quad * 32) + lane;
       const uint32_t row_addr = tmem_base + ((quad * 32u) << 16) + C::kACol;
-      // forward, nh a multiple of 64, ungrouped: M in shared memory once its
-      // bulk copy has landed (the copy left ahead of every tile load), read as
-      // 16-byte row vectors; otherwise the entries come from L2
-      bool msm = false;
-      if constexpr (!BWD) {
-        msm = p.m_bulk != 0;
-        if (msm) wait_bar(bar_m, 0, abort_flag, (kRoleEpilogue << 8) | kBarM);
-      }
+      // Ungrouped M with a 16-byte-aligned start: M in shared memory once its
+      // bulk copy has landed (the copy left ahead of every tile load);
+      // otherwise the entries come from L2.
+      const bool msm = p.m_bulk != 0;
+      if (msm) wait_bar(bar_m, 0, abort_flag, (kRoleEpilogue << 8) | kBarM);
+      const float* Msm = reinterpret_cast<const float*>(gbase + C::kOffOut);  // [nh][nh]
       if constexpr (STK) {
         // stacked A in shared memory (128-byte-swizzled K-major rows, K = the
         // 64 heads): row m < 64 is M^T_hi row m, row 64 + h is M^T_lo row h
         const MixLine col(p, m & 63, false);
         float v[64];
 #pragma unroll
-        for (int q = 0; q < 64; ++q) v[q] = col.at(q);
+        for (int q = 0; q < 64; ++q) v[q] = msm ? Msm[q * 64 + (m & 63)] : col.at(q);
         uint32_t w[32];
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
@@ -681,7 +680,16 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
         for (int i = 0; i < 2; ++i) {
           const int kh = i ^ kfirst;
           float v[64];
-          if (msm) {
+          if (msm && (p.nh & 63) != 0) {
+            // M[g][o] (forward) or M[o][f] (backward) from shared memory
+#pragma unroll
+            for (int q = 0; q < 64; ++q) {
+              const unsigned o = static_cast<unsigned>(kh * 64 + q - pb);
+              v[q] = (live && o < static_cast<unsigned>(p.nh))
+                         ? Msm[BWD ? static_cast<int>(o) * p.nh + (m - pb) : (m - pb) * p.nh + static_cast<int>(o)]
+                         : 0.f;
+            }
+          } else if (msm && !BWD) {
             // nh % 64 == 0: this half lies wholly inside or outside the block
             const int o0 = kh * 64 - pb;  // first column of this half within the block
             if (live && o0 >= 0 && o0 < p.nh) {
@@ -703,7 +711,9 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
 #pragma unroll
             for (int q = 0; q < 64; ++q) {
               const unsigned o = static_cast<unsigned>(kh * 64 + q - pb);
-              v[q] = (live && o < static_cast<unsigned>(p.nh)) ? line.at(static_cast<int>(o)) : 0.f;
+              v[q] = (live && o < static_cast<unsigned>(p.nh))
+                         ? (msm ? Msm[static_cast<int>(o) * p.nh + (m - pb)] : line.at(static_cast<int>(o)))
+                         : 0.f;
             }
           }
           uint32_t whi[32], wlo[32];
@@ -1736,9 +1746,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
   // ------------------------------------------------------------ teardown
   // M's bulk copy must have landed before the CTA leaves (it has, unless the
   // CTA gave up early): bounded wait that ignores the abort flag
-  if constexpr (!BWD) {
-    if (p.m_bulk && threadIdx.x == 0) wait_bar_noabort(bar_m, 0);
-  }
+  if (p.m_bulk && threadIdx.x == 0) wait_bar_noabort(bar_m, 0);
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -2086,8 +2094,9 @@ extern "C" int invrope_postmix_fwd_ex(const void* O, const float* M, void* Y, in
   p.rows = sq * nh;
   p.log2_theta = std::log2(theta);
   p.n_static = s.n_tiles;
-  // M by one bulk copy at kernel start: 16-byte aligned, ungrouped, nh % 64 == 0
-  p.m_bulk = (aligned(M, 16) && gs == nh && nh % 64 == 0) ? 1 : 0;
+  // M by one bulk copy at kernel start: 16-byte aligned, ungrouped, a whole
+  // number of 16-byte units (nh even)
+  p.m_bulk = (aligned(M, 16) && gs == nh && nh % 2 == 0) ? 1 : 0;
   fill_freq(p.F, pe, theta);
   const int64_t grid = s.n_tiles < dev.sms ? s.n_tiles : dev.sms;
   postmix_kernel<false><<<static_cast<unsigned>(grid), KCfg<false>::kThreads, KCfg<false>::kSmemAlloc,
@@ -2172,7 +2181,10 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
     p.n_nope_ct = s.n_nope_ct;
     p.rows = sq * nh;
     p.log2_theta = std::log2(theta);
-    p.m_bulk = 0;  // the backward reads M from L2 (a bulk copy did not pay off there)
+    // The backward reads M from L2 (prefetched there): a bulk copy into shared
+    // memory ahead of the first tile cost the production shard 5-8 us (and
+    // gained nothing on the small configs). The kernel supports it (m_bulk).
+    p.m_bulk = 0;
     p.n_static = tail.n_static;
     p.n_tail = tail.n_tail;
     p.tail_na = tail.na;
