@@ -94,9 +94,13 @@ enum : unsigned { kBarFull = 1, kBarEmpty, kBarAccFull, kBarAccEmpty, kBarXFull,
 
 // WIDE (backward with one position per tile, nh > 64): 128-channel tiles, so
 // each head-mix MMA has N = 128 and a tile needs half as many of them.
-// STK (backward, nh = 64, pe block = one whole chunk): the stacked head mix,
-// with A = [M^T_hi ; M^T_lo] in shared memory so that TMEM holds two D2
-// buffers (the drain of one segment overlaps the next segment's dM chains).
+// STK (backward, nh = 64, pe block = one whole chunk): the stacked head mix.
+// Its dM share sums the tile's two positions in the MMAs themselves (M = 64
+// per position, one 64 x 64 accumulator), so two D2 buffers take 128 TMEM
+// columns (the drain of one segment overlaps the next segment's dM chains),
+// with A in TMEM as in the other kernels. Two output buffers measured ~1 us
+// faster than three, and a fifth input stage (the shared memory allows it)
+// ~2 us slower, at the production shard.
 template <bool BWD, bool WIDE = false, bool STK = false>
 struct KCfg {
   static_assert(!STK || (BWD && !WIDE), "the stacked mix is a 64-channel backward");
@@ -105,13 +109,15 @@ struct KCfg {
   static constexpr int kTensorTile = kChunks * kChunkBytes;
   static constexpr int kStageBytes = (BWD ? 2 : 1) * kTensorTile;   // input ring entry
   static constexpr int kStages = WIDE ? 2 : 4;           // input ring (bytes in flight alike)
-  static constexpr int kOutBufs = BWD ? 3 : 5;           // output ring of 64-channel chunks
-  static constexpr int kOutInflight = kOutBufs - 2;      // TMA stores left reading smem
+  static constexpr int kOutBufs = BWD ? (STK ? 2 : 3) : 5;  // output ring of 64-channel chunks
+  // TMA stores left reading shared memory (two buffers: one, waited after each store)
+  static constexpr int kOutInflight = kOutBufs > 3 ? kOutBufs - 2 : 1;
   static constexpr int kNumAcc = BWD ? (WIDE ? 2 : 4) : 3;
   static constexpr int kNumD2 = STK ? 2 : 1;
-  // TMEM columns: accumulators, then dM (bwd: one or two 128-column buffers),
-  // then (all but STK) A hi (64) and A lo (64)
+  // TMEM columns: accumulators, then dM (bwd: one 128-column buffer, or two of
+  // 64 columns for STK), then A hi (64) and A lo (64) (STK: 32 columns)
   static constexpr int kD2Col = kNumAcc * NC;
+  static constexpr int kD2Cols = STK ? 64 : 128;
   static constexpr int kACol = 384;
   static constexpr int kTmemCols = 512;
   // warps: 0 TMA producer, 1 MMA issuer, 2-5 epilogue, (6-9 transform,) last = TMA store
@@ -125,12 +131,9 @@ struct KCfg {
   // bwd, stacked mix: fp32 exchange rows between the epilogue warp pairs (64 x 256 B)
   static constexpr int kOffXch = kOffXlo + kXloBytes;
   static constexpr int kXchBytes = STK ? 64 * 256 : 0;
-  // STK: A = [M^T_hi ; M^T_lo], 128 rows of 64 bf16, 128-byte-swizzled K-major
-  static constexpr int kOffA = kOffXch + kXchBytes;
-  static constexpr int kABytes = STK ? kChunkBytes : 0;
   // rotation tables: positions per tile x 32 pairs (STK: 2 positions)
   static constexpr int kTabBytes = (STK ? 2 : kPosPerTileMax) * kMaxHalf * 8;
-  static constexpr int kOffTabEpi = kOffA + kABytes;
+  static constexpr int kOffTabEpi = kOffXch + kXchBytes;
   static constexpr int kOffTabXf = kOffTabEpi + kTabBytes;
   static constexpr int kOffFreq = kOffTabXf + (BWD ? kTabBytes : 0);
   static constexpr int kOffBars = kOffFreq + kMaxHalf * 8;
@@ -142,7 +145,7 @@ struct KCfg {
   static constexpr int kSmemBytes = kOffMisc + 192 + (BWD ? 128 : 0);
   static constexpr int kSmemAlloc = kSmemBytes + 1024;   // slack to align the base
   static_assert(kSmemAlloc <= 232448, "shared memory budget");
-  static_assert(kNumAcc * NC + (BWD ? kNumD2 * 128 : 0) <= (STK ? kTmemCols : kACol), "TMEM budget");
+  static_assert(kNumAcc * NC + (BWD ? kNumD2 * kD2Cols : 0) <= kACol, "TMEM budget");
   static_assert(kStages * kStageBytes >= 128 * 129 * 4, "dM partial reduction reuses the input ring");
   static_assert(kOutInflight >= 1, "at least one store in flight");
   static_assert(kOffFreq - kOffOut >= 128 * 128 * 4, "M is copied into the output ring and the buffers after it");
@@ -649,8 +652,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
       if (msm) wait_bar(bar_m, 0, abort_flag, (kRoleEpilogue << 8) | kBarM);
       const float* Msm = reinterpret_cast<const float*>(gbase + C::kOffOut);  // [nh][nh]
       if constexpr (STK) {
-        // stacked A in shared memory (128-byte-swizzled K-major rows, K = the
-        // 64 heads): row m < 64 is M^T_hi row m, row 64 + h is M^T_lo row h
+        // stacked A: lane m < 64 holds M^T_hi row m, lane 64 + h holds M^T_lo row h
         const MixLine col(p, m & 63, false);
         float v[64];
 #pragma unroll
@@ -661,10 +663,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
           const uint32_t hw = ptx::pack_bf16x2(v[2 * q], v[2 * q + 1]);
           w[q] = m < 64 ? hw : ptx::pack_bf16x2(v[2 * q] - ptx::bf16_lo_f32(hw), v[2 * q + 1] - ptx::bf16_hi_f32(hw));
         }
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          ptx::st_shared_v4(swz_unit_addr(base + C::kOffA, m, 8 * u), w[4 * u], w[4 * u + 1], w[4 * u + 2],
-                            w[4 * u + 3]);
+        ptx::tmem_st_x32(row_addr, w);
       } else {
         // A = blockdiag_P(M) (forward) or blockdiag_P(M^T) (backward): row m
         // (position m / nh, head m % nh) is nonzero on columns [pb, pb + nh) only
@@ -828,7 +827,10 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
       uint32_t d2_par = 0;
       int cur_b = 0;   // D2 buffer of the segment being issued
       int owe_b = -1;  // STK: buffer whose segment is complete once the pending pe tile's chain is out
-      // D2[b] += dY_tile * X_tile^T (both K-major, K = channels), plus dY_pe * X_lo^T on a pe tile
+      // D2[b] += dY_tile * X_tile^T (both K-major, K = channels), plus dY_pe * X_lo^T on a pe tile.
+      // STK: one M = 64 MMA per position into the same 64 x 64 accumulator
+      // (row m in TMEM lane 32 (m / 16) + m % 16), rows 64p.. of both operands
+      // 8 KB apart, so D2 holds the position sum itself.
       auto dm_chain = [&](int st, const Tile& x, int b) -> bool {
         if (b == d2_wait_b) {
           if (!wait_bar(bar_d2e(b), d2_par, abort_flag, (kRoleMma << 8) | kBarD2Empty)) return false;
@@ -836,10 +838,29 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
           d2_wait_b = -1;
         }
         const uint32_t sa = stage_addr(st);
-        const uint32_t d2 = tmem_base + C::kD2Col + static_cast<uint32_t>(b) * 128u;
+        const uint32_t d2 = tmem_base + C::kD2Col + static_cast<uint32_t>(b) * C::kD2Cols;
         uint32_t started = (d2_started >> b) & 1u;
-        const uint32_t idesc_dm = ptx::idesc_bf16_f32(128, 128, false, false);
         const uint32_t xa = sa + C::kTensorTile;
+        if constexpr (STK) {
+          const uint32_t idesc_dm = ptx::idesc_bf16_f32(64, 64, false, false);
+          for (uint32_t ps = 0; ps < 2; ++ps)
+            for (uint32_t kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = ptx::smem_desc_sw128(sa + ps * 8192u + kk * 32, 16, 1024);
+              const uint64_t bd = ptx::smem_desc_sw128(xa + ps * 8192u + kk * 32, 16, 1024);
+              ptx::tc_mma_ss(d2, ad, bd, idesc_dm, started);
+              started = 1;
+            }
+          d2_started |= 1u << b;
+          if (x.has_pe)
+            for (uint32_t ps = 0; ps < 2; ++ps)
+              for (uint32_t kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = ptx::smem_desc_sw128(sa + ps * 8192u + kk * 32, 16, 1024);
+                const uint64_t bd = ptx::smem_desc_sw128(base + C::kOffXlo + ps * 8192u + kk * 32, 16, 1024);
+                ptx::tc_mma_ss(d2, ad, bd, idesc_dm, 1);
+              }
+          return true;
+        }
+        const uint32_t idesc_dm = ptx::idesc_bf16_f32(128, 128, false, false);
         for (int k = 0; k < x.nch; ++k)
           for (uint32_t kk = 0; kk < 4; ++kk) {
             const uint64_t ad = ptx::smem_desc_sw128(sa + k * kChunkBytes + kk * 32, 16, 1024);
@@ -943,13 +964,12 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
         const uint32_t d_acc = tmem_base + static_cast<uint32_t>(acc) * acc_cols;
         if constexpr (STK) {
           // stacked: D[128 x 128] = [M^T_hi ; M^T_lo] * [tile rows 0-63 | tile rows 64-127],
-          // K = the 64 heads of a position (A K-major in shared memory); N block
-          // 1 sits 64 rows (8 KB) below N block 0
+          // K = the 64 heads of a position (A in TMEM); N block 1 sits 64 rows
+          // (8 KB) below N block 0
           const uint32_t idesc_stk = ptx::idesc_bf16_f32(128, 128, false, true);
           for (uint32_t ks = 0; ks < 4; ++ks) {
-            const uint64_t ad = ptx::smem_desc_sw128(base + C::kOffA + ks * 32, 16, 1024);
             const uint64_t bd = ptx::smem_desc_sw128(sa + ks * 2048, 64 * 128, 1024);
-            ptx::tc_mma_ss(d_acc, ad, bd, idesc_stk, ks != 0);
+            ptx::tc_mma_ts(d_acc, tmem_base + C::kACol + ks * 8, bd, idesc_stk, ks != 0);
           }
         } else {
           const uint32_t idesc_mix = ptx::idesc_bf16_f32(128, 64u * x.nch, false, true);
@@ -1431,55 +1451,29 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
         ptx::tc_fence_after();
         const uint32_t q4 = static_cast<uint32_t>(warp & 3);
         const int r = static_cast<int>(q4 * 32u) + lane;  // this thread's TMEM lane: D2 row r
-        const uint32_t taddr = tmem_base + ((q4 * 32u) << 16) + C::kD2Col + static_cast<uint32_t>(b) * 128u;
+        const uint32_t taddr = tmem_base + ((q4 * 32u) << 16) + C::kD2Col + static_cast<uint32_t>(b) * C::kD2Cols;
         const bool rok = r < p.R;
         const int nh = p.nh;
         const int pl = rok ? r / nh : 0, g = r - pl * nh;
         const int lo = pl * nh, hi = lo + nh;
         float* dst = p.ws + static_cast<int64_t>(slot) * nh * nh;
         if constexpr (STK) {
-          // nh = 64, two positions: row r's block row is columns [64 pl, 64 pl + 64)
-          // (pl is uniform per warp). Position 1's rows park theirs in X_lo
-          // (16-byte unit u of row g at u ^ (g & 15)), position 0's rows add
-          // them and write partial row g. The other D2 buffer takes the next
-          // segment meanwhile, so nothing waits for this hand-back.
-          float4* xch = reinterpret_cast<float4*>(gbase + C::kOffXlo);
-          if (pl == 1) {
-            for (int h2 = 0; h2 < 2; ++h2) {
-              uint32_t v[32];
-              ptx::tmem_ld_x32(taddr + 64u + 32u * h2, v);
-              ptx::tmem_ld_wait(v);
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                const int uu = 8 * h2 + u;
-                xch[g * 16 + (uu ^ (g & 15))] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                                                            __uint_as_float(v[4 * u + 2]),
-                                                            __uint_as_float(v[4 * u + 3]));
-              }
-            }
-          }
-          ptx::named_bar_sync(2, 128);
-          if (pl == 0) {
-            float4* drow = reinterpret_cast<float4*>(dst + static_cast<int64_t>(g) * 64);
-            for (int h2 = 0; h2 < 2; ++h2) {
-              uint32_t v[32];
-              ptx::tmem_ld_x32(taddr + 32u * h2, v);
-              ptx::tmem_ld_wait(v);
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                const int uu = 8 * h2 + u;
-                const float4 o = xch[g * 16 + (uu ^ (g & 15))];
-                drow[uu] = make_float4(__uint_as_float(v[4 * u]) + o.x, __uint_as_float(v[4 * u + 1]) + o.y,
-                                       __uint_as_float(v[4 * u + 2]) + o.z, __uint_as_float(v[4 * u + 3]) + o.w);
-              }
-            }
-          }
+          // D2 is the position-summed 64 x 64 block: row g in lane 32 (g / 16) +
+          // g % 16, so lanes 0-15 of each warp hold rows 16 q4 .. 16 q4 + 15.
+          // The other D2 buffer takes the next segment meanwhile, so nothing
+          // waits for this hand-back.
+          uint32_t v[64];
+          ptx::tmem_ld_x64(taddr, v);
+          ptx::tmem_ld_wait(v);
           ptx::tc_fence_before();
           ptx::mbar_arrive(bar_d2e(b));
-          ptx::named_bar_sync(2, 128);  // every row has read X_lo
-          for (uint32_t o = static_cast<uint32_t>(xr) * 16u; o < static_cast<uint32_t>(C::kXloBytes); o += 128u * 16u)
-            ptx::st_shared_v4(base + C::kOffXlo + o, 0u, 0u, 0u, 0u);
-          ptx::fence_proxy_async_smem();
+          if (lane < 16) {
+            float4* drow = reinterpret_cast<float4*>(dst + static_cast<int64_t>(q4 * 16u + lane) * 64);
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+              drow[u] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                    __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+          }
         } else if (p.P == 1) {
           // one position per tile: D2 row r is partial row r
           for (int j0 = 0; j0 < nh; j0 += 32) {
