@@ -487,12 +487,40 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
   auto acc_of = [&](uint32_t i) { return static_cast<int>(BWD ? i & ((1u << na_sh) - 1u) : i % NA); };
   auto acc_phase = [&](uint32_t i) { return BWD ? (i >> na_sh) & 1u : (i / NA) & 1u; };
 
+  // one input tile into stage st: its full barrier expects the bytes, then the
+  // 64-channel boxes (and, backward, O's boxes behind dY's)
+  auto load_tile = [&](int st, int64_t t) {
+    const Tile x = decode_tile<BWD, WIDE>(p, t);
+    INVROPE_DBG_CHECK(t >= 0 && t < p.n_tiles && x.row0 >= 0 && x.xa % 8 == 0 && x.xa < p.d &&
+                          (x.nch < 2 || (x.xb % 8 == 0 && x.xb < p.d)) && x.nch >= 1 && x.nch <= C::kChunks,
+                      2);
+    const uint32_t bytes = static_cast<uint32_t>(x.nch * p.R * 128 * (BWD ? 2 : 1));
+    ptx::mbar_arrive_expect_tx(bar_full(st), bytes);
+    const uint32_t sa = stage_addr(st);
+    // general pe tiles read all d channels; every other tile reads through
+    // tm_in0 / tm_in1 (clipped at channel nope under the general tiling)
+    const CUtensorMap* m0 = (kGen && x.kind == 2) ? &p.tm_in0_pe : &p.tm_in0;
+    for (int k = 0; k < x.nch; ++k) ptx::tma_load_2d(sa + k * kChunkBytes, m0, box_x(x, k), x.row0, bar_full(st));
+    if (BWD) {
+      const CUtensorMap* m1 = (kGen && x.kind == 2) ? &p.tm_in1_pe : &p.tm_in1;
+      for (int k = 0; k < x.nch; ++k)
+        ptx::tma_load_2d(sa + C::kTensorTile + k * kChunkBytes, m1, box_x(x, k), x.row0, bar_full(st));
+    }
+  };
+
+  const int64_t G = gridDim.x;
+  // forward: unused; backward: this CTA's static share of the first n_static tiles
+  const int64_t t_begin = p.n_static * blockIdx.x / G;
+  const int64_t t_end = p.n_static * (blockIdx.x + 1) / G;
+  // The first tile needs no work counter (forward: tile blockIdx.x; backward:
+  // the static share's first), so thread 0 loads it as soon as the barriers
+  // exist, ahead of the rest of the set-up.
+  const int64_t t_first = BWD ? t_begin : static_cast<int64_t>(blockIdx.x);
+  const bool early = BWD ? t_begin < t_end : t_first < p.n_tiles;
+
   // ------------------------------------------------------------ setup
-  // thread 0 (the TMA producer) issues the slot acquisition first; its result
-  // is needed only at the end of the barrier set-up
   bool sched_mine = false;
   const bool use_sched = !BWD || p.n_tail > 0;
-  if (use_sched && threadIdx.x == 0) sched_mine = sched_acquire(p.sched, launch_tag());
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(bar_full(s), 1);
@@ -523,10 +551,6 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
       }
     }
     *abort_flag = 0;
-    // take the launch's counter slot; if another launch still holds it, claim
-    // nothing from it and wind down (outputs undefined, fault recorded)
-    if (use_sched && !sched_mine)
-      record_fault(BWD ? INVROPE_FAULT_SCHED_BUSY_BWD : INVROPE_FAULT_SCHED_BUSY_FWD, abort_flag);
     ptx::fence_mbar_init();
     // M goes out first, ahead of every tile load (into the output ring, idle
     // until the first tile is mixed); the A build waits on it
@@ -534,6 +558,10 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
       const uint32_t mbytes = static_cast<uint32_t>(p.nh * p.gs * 4);
       ptx::mbar_arrive_expect_tx(bar_m, mbytes);
       ptx::bulk_load(base + C::kOffOut, p.M, mbytes, bar_m);
+    }
+    if (early) {
+      if (!BWD) stage_tile[0] = static_cast<int>(t_first);  // published by the load's barrier
+      load_tile(0, t_first);
     }
   }
   if (warp == 0 && lane == 0) {
@@ -552,7 +580,6 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
       for (int o = lane * 128; o < mbytes; o += 32 * 128) ptx::prefetch_l2(mb + o);
     __syncwarp();
   }
-  if (threadIdx.x < half && threadIdx.x < kMaxHalf) F[threadIdx.x] = p.F[threadIdx.x];
   // Rows >= R of every 64-channel box are never loaded and must read as 0
   // (the MMA's K range covers them).
   if (p.R < kRowsMax) {
@@ -563,14 +590,10 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
   }
   ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
+  __syncwarp();  // thread 0 ran the set-up alone: its warp meets the barrier converged
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-
-  const int64_t G = gridDim.x;
-  // forward: unused; backward: this CTA's static share of the first n_static tiles
-  const int64_t t_begin = p.n_static * blockIdx.x / G;
-  const int64_t t_end = p.n_static * (blockIdx.x + 1) / G;
 
   // Backward segments, in the order every role runs them: segment 0 is the
   // static share (dM partial slot blockIdx.x), then the tail blocks this CTA
@@ -637,6 +660,8 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
   // barrier 4 (all warps but the producer).
   if (warp != 0) {
     const int nthr = static_cast<int>(blockDim.x) - 32, tid = static_cast<int>(threadIdx.x) - 32;
+    // the rotation frequencies (epilogue and transform warps read them after barrier 4)
+    if (tid < half && tid < kMaxHalf) F[tid] = p.F[tid];
     if (warp >= 2 && warp < 6) {
       // A in TMEM: lane m holds row m; column kACol + hl*64 + j/2 holds the bf16
       // pair (j, j+1) of the hi (hl = 0) or lo (hl = 1) term, lower j in the
@@ -741,22 +766,33 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
-      // forward: the first tile is the block index, later ones are claimed
-      // from the launch's counter, one claim ahead. Backward: the static share,
+      // forward: the first two tiles are static (blockIdx.x, G + blockIdx.x),
+      // later ones are claimed from the launch's counter, one claim ahead. Backward: the static share,
       // then tail blocks claimed one segment ahead, each segment published to
       // the other roles before its first tile is loaded.
       // The next tail block is claimed a few tiles before the current segment
       // ends, so that the claims come in the order in which CTAs run out of
       // work (the claim's latency hides behind those tiles' loads).
       constexpr int64_t kClaimAhead = 3;
-      int64_t t_next = BWD ? t_begin : static_cast<int64_t>(blockIdx.x);
+      // Take the launch's counter slot (off the set-up's path: only the claims
+      // need it). If another launch still holds it, claim nothing from it and
+      // wind down (outputs undefined, fault recorded) once the first tile's
+      // copies have landed.
+      if (use_sched) sched_mine = sched_acquire(p.sched, launch_tag());
+      if (use_sched && !sched_mine) {
+        if (early) wait_bar_noabort(bar_full(0), 0);
+        record_fault(BWD ? INVROPE_FAULT_SCHED_BUSY_BWD : INVROPE_FAULT_SCHED_BUSY_FWD, abort_flag);
+      }
+      // stage 0 holds the first tile; the forward's second is static too
+      // (tile G + blockIdx.x), later ones come from the counter (2G + claim)
+      int64_t t_next = early ? t_first + (BWD ? 1 : G) : t_first;
       int64_t seg_end = t_end;
       uint32_t seg_k = 0;
       uint32_t claim = 0xffffffffu;
       bool claimed = false;
-      bool run = true;
-      if constexpr (BWD) run = !*abort_flag && seg_publish(0, t_begin, t_end, static_cast<int>(blockIdx.x));
-      for (uint32_t i = 0; run; ++i) {
+      bool run = !*abort_flag;
+      if constexpr (BWD) run = run && seg_publish(0, t_begin, t_end, static_cast<int>(blockIdx.x));
+      for (uint32_t i = early ? 1u : 0u; run; ++i) {
         const int st = static_cast<int>(i % S);
         const uint32_t ph = (i / S) & 1u;
         if constexpr (BWD) {
@@ -793,25 +829,10 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
             ptx::mbar_arrive(bar_full(st));
             break;
           }
-          t_next = static_cast<int64_t>(gridDim.x) + static_cast<int64_t>(atomicAdd(&p.sched->next, 1u));
+          t_next = 2 * G + static_cast<int64_t>(atomicAdd(&p.sched->next, 1u));
           stage_tile[st] = static_cast<int>(t);
         }
-        const Tile x = decode_tile<BWD, WIDE>(p, t);
-        INVROPE_DBG_CHECK(t >= 0 && t < p.n_tiles && x.row0 >= 0 && x.xa % 8 == 0 && x.xa < p.d &&
-                              (x.nch < 2 || (x.xb % 8 == 0 && x.xb < p.d)) && x.nch >= 1 && x.nch <= C::kChunks,
-                          2);
-        const uint32_t bytes = static_cast<uint32_t>(x.nch * p.R * 128 * (BWD ? 2 : 1));
-        ptx::mbar_arrive_expect_tx(bar_full(st), bytes);
-        const uint32_t sa = stage_addr(st);
-        // general pe tiles read all d channels; every other tile reads through
-        // tm_in0 / tm_in1 (clipped at channel nope under the general tiling)
-        const CUtensorMap* m0 = (kGen && x.kind == 2) ? &p.tm_in0_pe : &p.tm_in0;
-        for (int k = 0; k < x.nch; ++k) ptx::tma_load_2d(sa + k * kChunkBytes, m0, box_x(x, k), x.row0, bar_full(st));
-        if (BWD) {
-          const CUtensorMap* m1 = (kGen && x.kind == 2) ? &p.tm_in1_pe : &p.tm_in1;
-          for (int k = 0; k < x.nch; ++k)
-            ptx::tma_load_2d(sa + C::kTensorTile + k * kChunkBytes, m1, box_x(x, k), x.row0, bar_full(st));
-        }
+        load_tile(st, t);
       }
     }
     __syncwarp();  // the whole warp reaches the teardown barrier together
