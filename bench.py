@@ -294,7 +294,16 @@ def config_sweep(ir, dev, stream, peak):
     input is served from the 129 MB L2), algorithmic GB/s and the fraction of
     the measured copy peak; beside it the fp64 oracle's time for fwd + bwd on
     the host cores (all rows, or a leading block of rows scaled to the config;
-    the production shard's oracle time is the cpu_baseline run)."""
+    the production shard's oracle time is the cpu_baseline run).
+
+    A single call of a small config is bounded by fixed costs: the event pair
+    around one trivial kernel already reads ~6 us on this GPU. For the configs
+    whose inputs fit in the L2, `stream` adds the per-call device time of
+    back-to-back calls: the calls are queued behind a sleep kernel (so the host
+    enqueue time is not measured), rotate over enough input/output sets that a
+    set comes back only after >= 256 MB (twice the L2) of the other sets'
+    traffic (at most 64 sets: tiny stays L2-resident and says so), and one
+    event pair spans them all."""
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     res = {}
     for c in (W.TINY, W.MID, W.SWEEP_NH3, W.SWEEP_NH128, W.PROD):
@@ -325,12 +334,65 @@ def config_sweep(ir, dev, stream, peak):
             row[f"{name}_us"] = round(us, 2)
             row[f"{name}_gbs"] = round(gbs, 1)
             row[f"{name}_frac"] = round(gbs / peak, 4)
+        if c.fwd_bytes() < (128 << 20):
+            row["stream"] = stream_sweep(ir, dev, stream, c, peak)
         del O, dY, Y, dO, ws
         row["oracle"] = oracle_config(c) if c.name in CONFIG_ORACLE_ROWS else {"kind": "oracle"}
         res[c.name] = row
     del flush
     torch.cuda.empty_cache()
     return res
+
+
+def stream_sweep(ir, dev, stream, c, peak, calls_per_rep=64):
+    """Per-call device time of back-to-back forward / backward calls of config
+    `c` over rotating input sets (see config_sweep)."""
+    set_bytes = {"fwd": c.fwd_bytes(), "bwd": c.bwd_bytes()}
+    out = {}
+    for name in ("fwd", "bwd"):
+        nsets = min(64, 1 + -(-(256 << 20) // set_bytes[name]))
+        sets = []
+        for j in range(nsets):
+            cj = W.PostmixConfig(c.name, sq=c.sq, nh=c.nh, nope=c.nope, pe=c.pe, pos0=c.pos0, seed=c.seed + j)
+            O, dY, M = W.postmix_inputs(cj, device=dev)
+            res = torch.empty_like(O)
+            dM = torch.empty(c.nh, c.nh, dtype=torch.float32, device=dev)
+            ws = torch.empty(max(16, ir.invrope_postmix_bwd_workspace_bytes(c.sq, c.nh, c.nope, c.pe)),
+                             dtype=torch.uint8, device=dev) if name == "bwd" else None
+            sets.append((O, dY, M, res, dM, ws))
+        del O, dY, M, res, dM, ws
+
+        def call(j):
+            O, dY, M, res, dM, ws = sets[j % nsets]
+            if name == "fwd":
+                ir.invrope_postmix_fwd(O, M, c.pos0, c.nope, c.pe, c.theta, Y=res)
+            else:
+                ir.invrope_postmix_bwd(dY, O, M, c.pos0, c.nope, c.pe, c.theta, dO=res, dM=dM, workspace=ws)
+        for j in range(nsets):
+            call(j)
+        per = []
+        for _ in range(5):
+            torch.cuda.synchronize()
+            torch.cuda._sleep(int(2e9 * 30e-6 * calls_per_rep))  # covers the host's enqueue of the calls
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for j in range(calls_per_rep):
+                call(j)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            per.append(e0.elapsed_time(e1) * 1e3 / calls_per_rep)
+        us = statistics.median(per)
+        gbs = set_bytes[name] / (us * 1e-6) / 1e9
+        out[f"{name}_us"] = round(us, 2)
+        out[f"{name}_gbs"] = round(gbs, 1)
+        out[f"{name}_frac"] = round(gbs / peak, 4)
+        out[f"{name}_sets"] = nsets
+        del sets
+    out["l2"] = ("inputs L2-resident (64 sets of the config fit in L2)" if 63 * c.fwd_bytes() < (256 << 20)
+                 else "a set comes back after >= 256 MB of other sets' traffic")
+    out["calls"] = calls_per_rep
+    torch.cuda.empty_cache()
+    return out
 
 
 def oracle_config(c):

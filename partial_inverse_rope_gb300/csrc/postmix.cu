@@ -208,7 +208,7 @@ struct Tile {
 __device__ __forceinline__ int box_x(const Tile& x, int k) { return k == 0 ? x.xa : x.xb; }
 
 // Tile (rt, ct): row tile rt, channel tile ct.
-template <bool BWD, bool WIDE = false>
+template <bool BWD, bool WIDE = false, bool GEN = true>
 __device__ __forceinline__ Tile make_tile(const PostmixParams& p, int rt, int ct) {
   using C = KCfg<BWD, WIDE>;
   Tile x;
@@ -219,7 +219,8 @@ __device__ __forceinline__ Tile make_tile(const PostmixParams& p, int rt, int ct
   x.j = 0;
   x.np = 0;
   // the general tiling occurs in the forward and the 128-channel backward only
-  constexpr bool kGen = !BWD || WIDE;
+  // (GEN: the instantiation that takes it)
+  constexpr bool kGen = (!BWD || WIDE) && GEN;
   const bool gen = kGen && p.gen;
   if (!gen || ct < p.n_nope_ct) {
     x.c0 = x.ct * C::NC;
@@ -244,13 +245,13 @@ __device__ __forceinline__ Tile make_tile(const PostmixParams& p, int rt, int ct
 }
 
 // Tile t of the row-major (row tile, channel tile) order.
-template <bool BWD, bool WIDE = false>
+template <bool BWD, bool WIDE = false, bool GEN = true>
 __device__ __forceinline__ Tile decode_tile(const PostmixParams& p, int64_t t) {
   // 32-bit division: the host guarantees n_tiles < 2^31 (64-bit division here
   // sits on the MMA issuer's critical path once per tile and is slow)
   const uint32_t tu = static_cast<uint32_t>(t);
   const uint32_t rt = tu / static_cast<uint32_t>(p.n_ct);
-  return make_tile<BWD, WIDE>(p, static_cast<int>(rt), static_cast<int>(tu - rt * static_cast<uint32_t>(p.n_ct)));
+  return make_tile<BWD, WIDE, GEN>(p, static_cast<int>(rt), static_cast<int>(tu - rt * static_cast<uint32_t>(p.n_ct)));
 }
 
 __device__ __forceinline__ void record_fault(unsigned code, volatile int* abort_flag) {
@@ -417,12 +418,12 @@ struct MixLine {
   }
 };
 
-template <bool BWD, bool WIDE = false, bool STK = false>
+template <bool BWD, bool WIDE = false, bool STK = false, bool GEN = true>
 __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
     postmix_kernel(const __grid_constant__ PostmixParams p) {
   using C = KCfg<BWD, WIDE, STK>;
   // the general tiling's pair blocks occur in the forward and the 128-channel backward only
-  constexpr bool kGen = !BWD || WIDE;
+  constexpr bool kGen = (!BWD || WIDE) && GEN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -490,7 +491,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
   // one input tile into stage st: its full barrier expects the bytes, then the
   // 64-channel boxes (and, backward, O's boxes behind dY's)
   auto load_tile = [&](int st, int64_t t) {
-    const Tile x = decode_tile<BWD, WIDE>(p, t);
+    const Tile x = decode_tile<BWD, WIDE, GEN>(p, t);
     INVROPE_DBG_CHECK(t >= 0 && t < p.n_tiles && x.row0 >= 0 && x.xa % 8 == 0 && x.xa < p.d &&
                           (x.nch < 2 || (x.xb % 8 == 0 && x.xb < p.d)) && x.nch >= 1 && x.nch <= C::kChunks,
                       2);
@@ -968,7 +969,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
           ptx::tc_commit(bar_acc_full(acc));
           break;
         }
-        const Tile x = decode_tile<BWD, WIDE>(p, t);
+        const Tile x = decode_tile<BWD, WIDE, GEN>(p, t);
         INVROPE_DBG_CHECK(st < S && acc < NA && t >= 0 && t < p.n_tiles, 3);
         // The transform warps only see pe tiles; this thread has observed every
         // stage phase in order, so it tells them when the pe tile has landed.
@@ -1070,7 +1071,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
         if (!seg_read_group(seg_k, s_t, s_t1, sl, (kRoleEpilogue << 8) | kBarSeg, e == 0, seg_bc_epi, 1)) break;
         ++seg_k;
         if (s_t < 0) break;
-        const Tile x0 = decode_tile<BWD, WIDE>(p, s_t);
+        const Tile x0 = decode_tile<BWD, WIDE, GEN>(p, s_t);
         e_rt = x0.rt;
         e_ct = x0.ct;
       }
@@ -1115,7 +1116,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
         }
         break;
       }
-      const Tile x = BWD ? make_tile<BWD, WIDE>(p, e_rt, e_ct) : decode_tile<BWD, WIDE>(p, t);
+      const Tile x = BWD ? make_tile<BWD, WIDE, GEN>(p, e_rt, e_ct) : decode_tile<BWD, WIDE, GEN>(p, t);
       if (BWD && ++e_ct == p.n_ct) {
         e_ct = 0;
         ++e_rt;
@@ -1419,7 +1420,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
         // of a general pair block (stored directly by the epilogue)
         int nk = 1;
         if (BWD) {
-          const Tile xb = decode_tile<BWD, WIDE>(p, tb);
+          const Tile xb = decode_tile<BWD, WIDE, GEN>(p, tb);
           nk = (kGen && xb.kind == 2) ? 0 : xb.nch;
         }
         for (int kk = 0; kk < nk; ++kk, ++n) {
@@ -1435,7 +1436,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
             break;
           }
           const int k = BWD ? kk : ob_chunk[b];
-          const Tile x = decode_tile<BWD, WIDE>(p, t);
+          const Tile x = decode_tile<BWD, WIDE, GEN>(p, t);
           INVROPE_DBG_CHECK(b < OB && k < x.nch && x.kind != 2 && box_x(x, k) < p.d, 6);
           ptx::tma_store_2d(&p.tm_out, out_addr(b), box_x(x, k), x.row0);
           ptx::bulk_commit();
@@ -1599,7 +1600,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
         if (s_t0 < 0) break;
         int64_t t = s_t0;
       for (; t < s_t1; ++t, ++i) {
-        const Tile x = decode_tile<BWD, WIDE>(p, t);
+        const Tile x = decode_tile<BWD, WIDE, GEN>(p, t);
         if (!x.has_pe) continue;
         const int st = static_cast<int>(i % S);
         const uint32_t ph = (i / S) & 1u;
@@ -1970,14 +1971,14 @@ bool make_maps(PostmixParams* p, const Shape& s, const void* in0, const void* in
   return true;
 }
 
-template <bool BWD, bool WIDE = false, bool STK = false>
+template <bool BWD, bool WIDE = false, bool STK = false, bool GEN = true>
 int ensure_smem_attr(int device) {
   static std::mutex mu;
   static bool done[64] = {};
   std::lock_guard<std::mutex> lock(mu);
   if (device < 0 || device >= 64) return INVROPE_ERR_DEVICE;
   if (!done[device]) {
-    const cudaError_t err = cudaFuncSetAttribute(postmix_kernel<BWD, WIDE, STK>,
+    const cudaError_t err = cudaFuncSetAttribute(postmix_kernel<BWD, WIDE, STK, GEN>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  KCfg<BWD, WIDE, STK>::kSmemAlloc);
     if (err != cudaSuccess) return cuda_fail(err);
@@ -2166,7 +2167,10 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (grid > 0) {
     const bool wide = s.wide;
-    if ((st = wide        ? ensure_smem_attr<true, true>(dev.device)
+    // the 128-channel kernel comes in two builds: with the general tiling's
+    // pair blocks, and without (its code made the nh = 128 backward ~13 us slower)
+    if ((st = wide        ? (s.gen ? ensure_smem_attr<true, true, false, true>(dev.device)
+                                   : ensure_smem_attr<true, true, false, false>(dev.device))
               : s.stacked ? ensure_smem_attr<true, false, true>(dev.device)
                           : ensure_smem_attr<true>(dev.device)) != INVROPE_OK)
       return st;
@@ -2212,8 +2216,11 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
         (st = slot_take(g_sched_ring, &g_sched, dev.device, cs, &p.sched)) != INVROPE_OK)
       return st;
     fill_freq(p.F, pe, theta);
-    if (wide)
-      postmix_kernel<true, true>
+    if (wide && s.gen)
+      postmix_kernel<true, true, false, true>
+          <<<static_cast<unsigned>(grid), KCfg<true, true>::kThreads, KCfg<true, true>::kSmemAlloc, cs>>>(p);
+    else if (wide)
+      postmix_kernel<true, true, false, false>
           <<<static_cast<unsigned>(grid), KCfg<true, true>::kThreads, KCfg<true, true>::kSmemAlloc, cs>>>(p);
     else if (s.stacked)
       postmix_kernel<true, false, true><<<static_cast<unsigned>(grid), KCfg<true, false, true>::kThreads,
