@@ -521,7 +521,8 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
 
   // ------------------------------------------------------------ setup
   bool sched_mine = false;
-  const bool use_sched = !BWD || p.n_tail > 0;
+  // forward launches with more than two tiles per CTA, backward ones with tail blocks
+  const bool use_sched = p.sched != nullptr;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(bar_full(s), 1);
@@ -830,7 +831,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
             ptx::mbar_arrive(bar_full(st));
             break;
           }
-          t_next = 2 * G + static_cast<int64_t>(atomicAdd(&p.sched->next, 1u));
+          t_next = use_sched ? 2 * G + static_cast<int64_t>(atomicAdd(&p.sched->next, 1u)) : p.n_tiles;
           stage_tile[st] = static_cast<int>(t);
         }
         load_tile(st, t);
@@ -2089,8 +2090,13 @@ extern "C" int invrope_postmix_fwd_ex(const void* O, const float* M, void* Y, in
   p.out = static_cast<uint16_t*>(Y);
   p.M = M;
   p.ws = nullptr;
-  if ((st = slot_take(g_sched_ring, &g_sched, dev.device, reinterpret_cast<cudaStream_t>(stream), &p.sched)) !=
-      INVROPE_OK)
+  // The first two tiles of each CTA are static: a launch with no more tiles
+  // than that claims nothing and needs no work-counter slot.
+  const int64_t grid = s.n_tiles < dev.sms ? s.n_tiles : dev.sms;
+  p.sched = nullptr;
+  if (s.n_tiles > 2 * grid &&
+      (st = slot_take(g_sched_ring, &g_sched, dev.device, reinterpret_cast<cudaStream_t>(stream), &p.sched)) !=
+          INVROPE_OK)
     return st;
   p.sq = sq;
   p.pos0 = pos0;
@@ -2114,7 +2120,6 @@ extern "C" int invrope_postmix_fwd_ex(const void* O, const float* M, void* Y, in
   // number of 16-byte units (nh even)
   p.m_bulk = (aligned(M, 16) && gs == nh && nh % 2 == 0) ? 1 : 0;
   fill_freq(p.F, pe, theta);
-  const int64_t grid = s.n_tiles < dev.sms ? s.n_tiles : dev.sms;
   postmix_kernel<false><<<static_cast<unsigned>(grid), KCfg<false>::kThreads, KCfg<false>::kSmemAlloc,
                           reinterpret_cast<cudaStream_t>(stream)>>>(p);
   return check_launch();

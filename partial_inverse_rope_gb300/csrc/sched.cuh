@@ -45,13 +45,16 @@ __device__ __forceinline__ bool sched_acquire(SchedSlot* s, unsigned long long t
 
 // Once per block that acquired the slot, after its last claim: the last of the
 // launch's nblocks blocks returns the counters to zero and frees the slot.
+// Each block's claims are performed before its done count (fence), so the
+// last block sees no claim still in flight and resets with plain stores,
+// ordered before the slot is freed.
 __device__ __forceinline__ void sched_release(SchedSlot* s, unsigned int nblocks) {
   __threadfence();
   if (atomicAdd(&s->done, 1u) == nblocks - 1u) {
-    atomicExch(&s->next, 0u);
-    atomicExch(&s->done, 0u);
+    *reinterpret_cast<volatile unsigned int*>(&s->next) = 0u;
+    *reinterpret_cast<volatile unsigned int*>(&s->done) = 0u;
     __threadfence();
-    atomicExch(&s->owner, 0ull);
+    *reinterpret_cast<volatile unsigned long long*>(&s->owner) = 0ull;
   }
 }
 
