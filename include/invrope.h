@@ -41,8 +41,9 @@
  *       . the 8 MiB scratch array of invrope_postmix_bwd_noalloc (see there
  *         for how calls share it and must be ordered).
  *     Work-counter slots: a forward launch with at most two tiles per
- *     thread block claims nothing and takes no slot. Otherwise an eager
- *     launch takes the next of 256 slots in turn, a launch made while its stream is being captured into a CUDA
+ *     thread block, or a remap with no more chunks than thread blocks,
+ *     claims nothing and takes no slot. Otherwise an eager launch takes the
+ *     next of 256 slots in turn, a launch made while its stream is being captured into a CUDA
  *     graph the next of 256 other slots, which it keeps on every replay. A
  *     launch's thread blocks take their slot only when it is free or held by
  *     their own launch; the last block frees it. A launch that finds its
@@ -292,8 +293,8 @@ int invrope_take_device_fault(int* fault);
  * Test hook (library infrastructure, not an operation of the pages): marks
  * the work-counter slot that the next eager slot-taking forward (which = 0:
  * more than two tiles per thread block, or a backward that hands out tail
- * blocks) or KV remap (which = 1) launch on the current device will take as
- * held by the launch
+ * blocks) or slot-taking KV remap (which = 1: more chunks than thread
+ * blocks) launch on the current device will take as held by the launch
  * tag `owner` (a synchronous host-to-device copy). With a non-zero owner
  * that no launch has, that next launch must find the slot busy, record
  * INVROPE_FAULT_SCHED_BUSY_FWD / _REMAP and leave its output undefined;

@@ -80,12 +80,13 @@ __global__ void __launch_bounds__(kThreads) kv_remap_kernel(const V* in, V* out,
   const int64_t nchunks = (n + kChunk - 1) / kChunk;
   // Thread 0 takes the launch's counter slot along with its first claim. A
   // block that finds the slot held by another launch still in flight does its
-  // static first chunk, claims nothing and records a fault.
+  // static first chunk, claims nothing and records a fault. A launch with no
+  // more chunks than blocks has no slot (sched == nullptr) and claims nothing.
   bool mine = false;
   // first chunk = block index; each later one is claimed while the current one streams
   for (int64_t ch = blockIdx.x; ch < nchunks;) {
     if (threadIdx.x == 0) {
-      if (ch == static_cast<int64_t>(blockIdx.x)) {
+      if (sched != nullptr && ch == static_cast<int64_t>(blockIdx.x)) {
         mine = sched_acquire(sched, launch_tag());
         if (!mine) atomicCAS(&g_remap_fault, 0u, static_cast<unsigned>(INVROPE_FAULT_SCHED_BUSY_REMAP));
       }
@@ -121,12 +122,16 @@ SlotRing g_remap_ring;
 template <typename V>
 int launch(const void* in, void* out, int64_t n, int64_t seg, uint64_t skv, const DeviceInfo& dev,
            cudaStream_t s) {
-  SchedSlot* sched = nullptr;
-  const int st = slot_take(g_remap_ring, &g_remap_sched, dev.device, s, &sched);
-  if (st != INVROPE_OK) return st;
   const int64_t nchunks = (n + kChunk - 1) / kChunk;
   const int64_t slots = static_cast<int64_t>(dev.sms) * 8;
   const int64_t grid = nchunks < slots ? nchunks : slots;
+  // a work-counter slot only when there is something to claim beyond the
+  // first chunk of each block
+  SchedSlot* sched = nullptr;
+  if (nchunks > grid) {
+    const int st = slot_take(g_remap_ring, &g_remap_sched, dev.device, s, &sched);
+    if (st != INVROPE_OK) return st;
+  }
   if (seg >= kChunk)
     kv_remap_kernel<V, true><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(
         static_cast<const V*>(in), static_cast<V*>(out), n, seg, skv, sched);

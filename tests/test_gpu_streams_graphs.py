@@ -141,11 +141,16 @@ def test_busy_slot_is_reported_not_shared(which):
     claim nothing from it and record the busy-slot code. Taking the fault frees
     every slot, and the next call gives the bits of a plain call again. The
     backward takes a slot (from the forward's slots) when it hands out tail
-    blocks, as at 4096 positions of 64 heads."""
+    blocks, as at 4096 positions of 64 heads; the forward and the remap when
+    they have more work than their first tile or chunk per thread block."""
     case = _case(43)
-    O, dY, M, idx = case
+    O, dY, M, _ = case
     _, _, nope, pe = SHAPE
     Ob, dYb, Mb = make_inputs(4096, 64, 448, 64, seed=44)
+    # a remap takes a slot only when it has more chunks than thread blocks:
+    # 2048 rows x 8192 entries (4M 16-byte vectors, 2048 chunks of 2048)
+    g = torch.Generator(device="cuda").manual_seed(45)
+    idx = torch.randint(-1, 4096, (4 * 512, 8192), generator=g, device="cuda", dtype=torch.int32)
 
     def call():
         if which == "fwd":
