@@ -170,3 +170,39 @@ def test_busy_slot_is_reported_not_shared(which):
     for _ in range(3):
         assert torch.equal(call(), ref)
     assert ir.invrope_take_device_fault() == 0
+
+
+@pytest.mark.parametrize("which", ["fwd", "remap"])
+def test_small_launches_take_no_slot(which):
+    """A forward with at most two tiles per thread block (the tiny shape) and a
+    remap with no more chunks than thread blocks claim nothing and take no
+    work-counter slot: with the next slot marked busy they still run
+    correctly and record no fault, and the next slot-taking launch is the
+    one that finds it busy."""
+    O, dY, M = make_inputs(128, 4, 48, 16, seed=46)
+    small_idx = torch.randint(-1, 4096, (4 * 64, 64), device="cuda", dtype=torch.int32,
+                              generator=torch.Generator(device="cuda").manual_seed(46))
+    big = _case(47)
+    big_idx = torch.randint(-1, 4096, (4 * 512, 8192), device="cuda", dtype=torch.int32,
+                            generator=torch.Generator(device="cuda").manual_seed(47))
+    _, _, nope, pe = SHAPE
+
+    def small():
+        if which == "fwd":
+            return ir.invrope_postmix_fwd(O, M, 3, 48, 16)
+        return ir.kv_idx_local_to_global(small_idx, 64, 4096)
+
+    def large():
+        if which == "fwd":
+            return ir.invrope_postmix_fwd(big[0], big[2], 7, nope, pe)
+        return ir.kv_idx_local_to_global(big_idx, 512, 4096)
+
+    ref = small()
+    assert ir.invrope_take_device_fault() == 0
+    ir.invrope_debug_occupy_next_slot(which, (1 << 63) + 4321)
+    for _ in range(3):
+        assert torch.equal(small(), ref)
+    assert ir.invrope_take_device_fault() == 0  # the slot is still marked: nothing took it
+    large()  # takes the marked slot: finds it busy
+    want = binding.INVROPE_FAULT_SCHED_BUSY_FWD if which == "fwd" else binding.INVROPE_FAULT_SCHED_BUSY_REMAP
+    assert ir.invrope_take_device_fault() == want
