@@ -836,6 +836,9 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
         }
         load_tile(st, t);
       }
+      // every claim of this CTA is made: count it done on the slot now (the
+      // launch's last CTA to do so frees it), off the kernel's final path
+      if (use_sched && sched_mine) sched_release(p.sched, gridDim.x);
     }
     __syncwarp();  // the whole warp reaches the teardown barrier together
   } else if (warp == 1) {
@@ -1770,7 +1773,6 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, C::kTmemCols);
   }
-  if (use_sched && threadIdx.x == 0 && sched_mine) sched_release(p.sched, gridDim.x);
 }
 
 // dM[o] = sum of the CTA partials ws[c][src(o)] (each [nh, nh]) in a fixed
