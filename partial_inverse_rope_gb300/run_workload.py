@@ -39,7 +39,8 @@ def main(argv=None):
                     help="take sq/nh/nope/pe/pos0 from a named config")
     ap.add_argument("--time", action="store_true", help="time each call (median over --reps)")
     ap.add_argument("--host-cost", type=int, default=0, metavar="N",
-                    help="host wall time per call over N back-to-back enqueues")
+                    help="host wall time per call over N back-to-back enqueues (keep N <= ~300: "
+                         "the launches must fit the stream's queue, or the host waits for the GPU)")
     args = ap.parse_args(argv)
 
     ops = [o.strip() for o in args.ops.split(",") if o.strip()]
@@ -116,6 +117,16 @@ def host_cost(ops, c, O, dY, M, Y, dO, dM, ws, R, idx, out, n):
     if idx is not None:
         argsets["remap"] = (lib.kv_idx_local_to_global, (idx.data_ptr(), out.data_ptr(), idx.shape[0],
                                                          idx.shape[1], R.sq, R.seqlen_kv, stream))
+    # the same calls with an argument the library rejects first thing (sq or
+    # rows < 0): the ctypes marshalling of these argument lists alone
+    rejects = {
+        "fwd": (-1,) + argsets["fwd"][1][4:],
+        "bwd": (-1,) + argsets["bwd"][1][8:],
+    }
+    rejects["fwd"] = argsets["fwd"][1][:3] + rejects["fwd"]
+    rejects["bwd"] = argsets["bwd"][1][:7] + rejects["bwd"]
+    if idx is not None:
+        rejects["remap"] = argsets["remap"][1][:2] + (-1,) + argsets["remap"][1][3:]
     for op in ops:
         fn, a = argsets[op]
         for _ in range(10):
@@ -130,13 +141,17 @@ def host_cost(ops, c, O, dY, M, Y, dO, dM, ws, R, idx, out, n):
             fn(*a)
         t1 = time.perf_counter()
         torch.cuda.synchronize()
-        # the ctypes call itself, on a C-ABI function that returns at once
+        # the same argument list rejected at once: ctypes marshalling + the
+        # first argument check, so the library's own host time is the difference
+        ra = rejects[op]
+        assert fn(*ra) != 0
         t2 = time.perf_counter()
         for _ in range(n):
-            lib.invrope_last_cuda_error()
+            fn(*ra)
         t3 = time.perf_counter()
-        print(f"{c.name} {op}: host {1e6 * (t1 - t0) / n:.2f} us per call over {n} enqueues "
-              f"(ctypes round trip alone {1e6 * (t3 - t2) / n:.2f} us)")
+        full, marshal = 1e6 * (t1 - t0) / n, 1e6 * (t3 - t2) / n
+        print(f"{c.name} {op}: host {full:.2f} us per call over {n} enqueues through ctypes; "
+              f"the same call rejected at its first check {marshal:.2f} us; library {full - marshal:.2f} us")
 
 
 if __name__ == "__main__":
