@@ -150,7 +150,9 @@ struct KCfg {
   static_assert(kNumAcc * NC + (BWD ? kNumD2 * kD2Cols : 0) <= kACol, "TMEM budget");
   static_assert(kStages * kStageBytes >= 128 * 129 * 4, "dM partial reduction reuses the input ring");
   static_assert(kOutInflight >= 1, "at least one store in flight");
-  static_assert(kOffFreq - kOffOut >= 128 * 128 * 4, "M is copied into the output ring and the buffers after it");
+  // the forward's bulk copy of M lands in the output ring and the buffers
+  // after it (the backward copies M only when it fits in the ring itself)
+  static_assert(BWD || kOffFreq - kOffOut >= 128 * 128 * 4, "M is copied into the output ring and the buffers after it");
 };
 
 struct PostmixParams {
@@ -2215,10 +2217,14 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
     p.n_nope_ct = s.n_nope_ct;
     p.rows = sq * nh;
     p.log2_theta = std::log2(theta);
-    // The backward reads M from L2 (prefetched there): a bulk copy into shared
-    // memory ahead of the first tile cost the production shard 5-8 us (and
-    // gained nothing on the small configs). The kernel supports it (m_bulk).
-    p.m_bulk = 0;
+    // M by one bulk copy at kernel start, as in the forward (it lands in the
+    // output ring, idle until the first tile is mixed), when it fits there:
+    // the X_lo buffer behind the ring is zeroed while the copy may still be
+    // landing. Otherwise (nh = 128) the A build reads M from L2.
+    const int out_ring = (wide ? KCfg<true, true>::kOutBufs
+                               : s.stacked ? KCfg<true, false, true>::kOutBufs : KCfg<true>::kOutBufs) *
+                         kChunkBytes;
+    p.m_bulk = (aligned(M, 16) && gs == nh && nh % 2 == 0 && nh * gs * 4 <= out_ring) ? 1 : 0;
     p.n_static = tail.n_static;
     p.n_tail = tail.n_tail;
     p.tail_na = tail.na;
