@@ -85,7 +85,8 @@ namespace {
 constexpr int kRowsMax = 128;                            // MMA M = rows of a tile
 constexpr int kChunkCols = 64;                           // channels per swizzle row
 constexpr int kChunkBytes = kRowsMax * kChunkCols * 2;   // one 64-channel box, 16 KB
-constexpr int kPosPerTileMax = 32;                       // caps the cos/sin table
+constexpr int kPosPerTileMax = 32;                       // caps the cos/sin table (backward)
+constexpr int kPosPerTileMaxFwd = 64;                    // the forward's (one table, more room)
 constexpr int kMaxHalf = 32;                             // pe / 2 <= 32
 constexpr uint64_t kWaitLimitNs = 2000000000ull;         // bounded waits: 2 s
 
@@ -134,7 +135,7 @@ struct KCfg {
   static constexpr int kOffXch = kOffXlo + kXloBytes;
   static constexpr int kXchBytes = STK ? 64 * 256 : 0;
   // rotation tables: positions per tile x 32 pairs (STK: 2 positions)
-  static constexpr int kTabBytes = (STK ? 2 : kPosPerTileMax) * kMaxHalf * 8;
+  static constexpr int kTabBytes = (STK ? 2 : BWD ? kPosPerTileMax : kPosPerTileMaxFwd) * kMaxHalf * 8;
   static constexpr int kOffTabEpi = kOffXch + kXchBytes;
   static constexpr int kOffTabXf = kOffTabEpi + kTabBytes;
   static constexpr int kOffFreq = kOffTabXf + (BWD ? kTabBytes : 0);
@@ -1943,7 +1944,8 @@ int check_shape(int64_t sq, int nh, int nope, int pe, bool bwd, Shape* s) {
   s->stacked = bwd && nh == 64 && pe == kChunkCols && nope % kChunkCols == 0;
   s->wide = bwd && !s->stacked && (s->gen || sq * nh * d * 2 >= (int64_t(1) << 20));
   const int nc = (!bwd || s->wide) ? 2 * kChunkCols : kChunkCols;
-  s->P = 128 / nh < kPosPerTileMax ? 128 / nh : kPosPerTileMax;
+  const int pmax = bwd ? kPosPerTileMax : kPosPerTileMaxFwd;
+  s->P = 128 / nh < pmax ? 128 / nh : pmax;
   s->R = s->P * nh;
   // tail blocks: the stacked kernel, whose double-buffered D2 makes segment
   // changes free (the 128-channel kernel's CTAs finish within ~25 us of each
