@@ -85,8 +85,8 @@ namespace {
 constexpr int kRowsMax = 128;                            // MMA M = rows of a tile
 constexpr int kChunkCols = 64;                           // channels per swizzle row
 constexpr int kChunkBytes = kRowsMax * kChunkCols * 2;   // one 64-channel box, 16 KB
-constexpr int kPosPerTileMax = 32;                       // caps the cos/sin table (backward)
-constexpr int kPosPerTileMaxFwd = 64;                    // the forward's (one table, more room)
+constexpr int kPosPerTileMax = 32;     // caps the cos/sin tables (backward with pair blocks)
+constexpr int kPosPerTileMaxFwd = 64;  // every other build (forward: one table; backward: one X_lo box)
 constexpr int kMaxHalf = 32;                             // pe / 2 <= 32
 constexpr uint64_t kWaitLimitNs = 2000000000ull;         // bounded waits: 2 s
 
@@ -104,7 +104,10 @@ enum : unsigned { kBarFull = 1, kBarEmpty, kBarAccFull, kBarAccEmpty, kBarXFull,
 // with A in TMEM as in the other kernels. Two output buffers measured ~1 us
 // faster than three, and a fifth input stage (the shared memory allows it)
 // ~2 us slower, at the production shard.
-template <bool BWD, bool WIDE = false, bool STK = false>
+// PAIRS: the build handles the general tiling's pair blocks (the forward, and
+// the 128-channel backward built with them); those need a second X_lo box, so
+// the backward builds without them have room for 64-position rotation tables.
+template <bool BWD, bool WIDE = false, bool STK = false, bool PAIRS = !BWD || WIDE>
 struct KCfg {
   static_assert(!STK || (BWD && !WIDE), "the stacked mix is a 64-channel backward");
   static constexpr int NC = (BWD && !WIDE) ? 64 : 128;   // channels per tile
@@ -130,12 +133,12 @@ struct KCfg {
   static constexpr int kOffStage = 0;
   static constexpr int kOffOut = kOffStage + kStages * kStageBytes;
   static constexpr int kOffXlo = kOffOut + kOutBufs * kChunkBytes;
-  static constexpr int kXloBytes = BWD ? kChunks * kChunkBytes : 0;
+  static constexpr int kXloBytes = BWD ? (PAIRS ? kChunks : 1) * kChunkBytes : 0;
   // bwd, stacked mix: fp32 exchange rows between the epilogue warp pairs (64 x 256 B)
   static constexpr int kOffXch = kOffXlo + kXloBytes;
   static constexpr int kXchBytes = STK ? 64 * 256 : 0;
   // rotation tables: positions per tile x 32 pairs (STK: 2 positions)
-  static constexpr int kTabBytes = (STK ? 2 : BWD ? kPosPerTileMax : kPosPerTileMaxFwd) * kMaxHalf * 8;
+  static constexpr int kTabBytes = (STK ? 2 : (BWD && PAIRS) ? kPosPerTileMax : kPosPerTileMaxFwd) * kMaxHalf * 8;
   static constexpr int kOffTabEpi = kOffXch + kXchBytes;
   static constexpr int kOffTabXf = kOffTabEpi + kTabBytes;
   static constexpr int kOffFreq = kOffTabXf + (BWD ? kTabBytes : 0);
@@ -424,9 +427,9 @@ struct MixLine {
 };
 
 template <bool BWD, bool WIDE = false, bool STK = false, bool GEN = true>
-__global__ void __launch_bounds__(KCfg<BWD, WIDE, STK>::kThreads, 1)
+__global__ void __launch_bounds__(KCfg<BWD, WIDE, STK, (!BWD || WIDE) && GEN>::kThreads, 1)
     postmix_kernel(const __grid_constant__ PostmixParams p) {
-  using C = KCfg<BWD, WIDE, STK>;
+  using C = KCfg<BWD, WIDE, STK, (!BWD || WIDE) && GEN>;
   // the general tiling's pair blocks occur in the forward and the 128-channel backward only
   constexpr bool kGen = (!BWD || WIDE) && GEN;
   extern __shared__ uint8_t smem_raw[];
@@ -1944,7 +1947,7 @@ int check_shape(int64_t sq, int nh, int nope, int pe, bool bwd, Shape* s) {
   s->stacked = bwd && nh == 64 && pe == kChunkCols && nope % kChunkCols == 0;
   s->wide = bwd && !s->stacked && (s->gen || sq * nh * d * 2 >= (int64_t(1) << 20));
   const int nc = (!bwd || s->wide) ? 2 * kChunkCols : kChunkCols;
-  const int pmax = bwd ? kPosPerTileMax : kPosPerTileMaxFwd;
+  const int pmax = (bwd && s->gen) ? kPosPerTileMax : kPosPerTileMaxFwd;
   s->P = 128 / nh < pmax ? 128 / nh : pmax;
   s->R = s->P * nh;
   // tail blocks: the stacked kernel, whose double-buffered D2 makes segment
@@ -1995,7 +1998,7 @@ int ensure_smem_attr(int device) {
   if (!done[device]) {
     const cudaError_t err = cudaFuncSetAttribute(postmix_kernel<BWD, WIDE, STK, GEN>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 KCfg<BWD, WIDE, STK>::kSmemAlloc);
+                                                 KCfg<BWD, WIDE, STK, (!BWD || WIDE) && GEN>::kSmemAlloc);
     if (err != cudaSuccess) return cuda_fail(err);
     done[device] = true;
   }
@@ -2243,8 +2246,8 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
       postmix_kernel<true, true, false, true>
           <<<static_cast<unsigned>(grid), KCfg<true, true>::kThreads, KCfg<true, true>::kSmemAlloc, cs>>>(p);
     else if (wide)
-      postmix_kernel<true, true, false, false>
-          <<<static_cast<unsigned>(grid), KCfg<true, true>::kThreads, KCfg<true, true>::kSmemAlloc, cs>>>(p);
+      postmix_kernel<true, true, false, false><<<static_cast<unsigned>(grid), KCfg<true, true, false, false>::kThreads,
+                                                 KCfg<true, true, false, false>::kSmemAlloc, cs>>>(p);
     else if (s.stacked)
       postmix_kernel<true, false, true><<<static_cast<unsigned>(grid), KCfg<true, false, true>::kThreads,
                                           KCfg<true, false, true>::kSmemAlloc, cs>>>(p);
