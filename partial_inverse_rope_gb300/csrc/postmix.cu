@@ -196,8 +196,6 @@ struct PostmixParams {
   // partial slot G + b.
   int64_t n_static;
   int n_tail, tail_na, tail_ba, tail_nb, tail_bb, tail_bc;
-  int pe_every_tile;   // bwd, not stacked: every tile holds pe channels (d <= 128, or nope < 8 under
-                       // the general tiling)
 };
 
 // kind 0: a tile of the regular tiling (channels c0 + 64 k, TMA-stored);
@@ -973,12 +971,16 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK, (!BWD || WIDE) && GEN>::k
           }
           t = s_t++;
         }
-        // When every tile holds pe channels, the previous tile's dM chain goes
+        // Backward but the stacked kernel: the previous pe tile's dM chain goes
         // out as soon as its X is formed, before this tile's data is waited
-        // for: its stage is then free again while this one loads (issued one
-        // tile late instead, it held its stage until the next tile had landed,
-        // leaving one load in flight).
-        if (BWD && p.pe_every_tile && pend_st >= 0 && !flush_pending()) break;
+        // for, so that its stage is free again while this one loads (issued
+        // after this tile's head mix instead, it held its stage until this
+        // tile had landed, and with two stages that left one load in flight:
+        // nh = 128 535 -> 507 us, [65536, 16, 64 + 64] 203 -> 150 us). The
+        // stacked kernel keeps the later place (134 vs 142 us at
+        // [16384, 64, 0 + 64]; the same at the production shard). The order is
+        // fixed either way, so dM stays reproducible.
+        if (BWD && !STK && pend_st >= 0 && !flush_pending()) break;
         if (!wait_bar(bar_full(st), ph, abort_flag, (kRoleMma << 8) | kBarFull)) break;
         if (!BWD) t = static_cast<int64_t>(stage_tile[st]);
         if (!BWD && t < 0) {
@@ -2240,9 +2242,6 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
     p.m_bulk = (aligned(M, 16) && gs == nh && nh % 2 == 0 && nh * gs * 4 <= out_ring) ? 1 : 0;
     p.n_static = tail.n_static;
     p.n_tail = tail.n_tail;
-    // (not the stacked kernel: at d = 64 its two D2 buffers keep the chain's
-    // usual place ahead, 134 vs 142 us at [16384, 64, 0 + 64])
-    p.pe_every_tile = (!s.stacked && (s.gen ? s.n_nope_ct == 0 : s.n_ct == 1)) ? 1 : 0;
     p.tail_na = tail.na;
     p.tail_ba = tail.ba;
     p.tail_nb = tail.nb;
