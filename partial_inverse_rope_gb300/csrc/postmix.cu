@@ -977,9 +977,9 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK, (!BWD || WIDE) && GEN>::k
         // after this tile's head mix instead, it held its stage until this
         // tile had landed, and with two stages that left one load in flight:
         // nh = 128 535 -> 507 us, [65536, 16, 64 + 64] 203 -> 150 us). The
-        // stacked kernel keeps the later place (134 vs 142 us at
-        // [16384, 64, 0 + 64]; the same at the production shard). The order is
-        // fixed either way, so dM stays reproducible.
+        // stacked kernel keeps the later place (4 stages; 134 vs 142 us at
+        // [16384, 64, 0 + 64], 484 vs 486 us at the production shard). The
+        // order is fixed either way, so dM stays reproducible.
         if (BWD && !STK && pend_st >= 0 && !flush_pending()) break;
         if (!wait_bar(bar_full(st), ph, abort_flag, (kRoleMma << 8) | kBarFull)) break;
         if (!BWD) t = static_cast<int64_t>(stage_tile[st]);
