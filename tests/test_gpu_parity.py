@@ -84,6 +84,10 @@ SHAPES = [
     (20, 64, 2, 254, 1, 1e4),         # 127 pairs, 64 heads
     (40, 7, 220, 76, 2**31 + 5, 5e5), # unaligned pairs, positions beyond 2^31, another base
     (131, 100, 448, 72, 8, 1e4),      # 36 pairs (a 4-pair second block), 100 heads
+    # 128-channel backward tiles with many positions per tile (tensors of 1 MiB or more)
+    (3000, 2, 448, 64, 1, 1e4),       # 64 positions per tile, R = 128
+    (5000, 1, 448, 64, 0, 1e4),       # 64 positions per tile, R = 64
+    (2100, 3, 160, 32, 3, 1e4),       # 42 positions (R = 126), pe tile every second tile
 ]
 
 
@@ -182,6 +186,21 @@ def test_bitwise_repeatable():
         assert torch.equal(Y, outs[0][0])
         assert torch.equal(dO, outs[0][1])
         assert torch.equal(dM, outs[0][2])
+
+
+@pytest.mark.parametrize("sq,nh,nope,pe", [(1024, 128, 448, 64), (4096, 2, 160, 32)])
+def test_wide_backward_bitwise_repeatable(sq, nh, nope, pe):
+    """The 128-channel backward issues a pe tile's dM chain before the next
+    tile's data is waited for: the issue order is still fixed by the tile
+    sequence, so repeated calls give the same bits."""
+    O, dY, M = make_inputs(sq, nh, nope, pe, seed=21)
+    dO0, dM0 = ir.invrope_postmix_bwd(dY, O, M, 5, nope, pe)
+    for _ in range(5):
+        dO, dM = ir.invrope_postmix_bwd(dY, O, M, 5, nope, pe)
+        assert torch.equal(dO, dO0)
+        assert torch.equal(dM, dM0)
+    torch.cuda.synchronize()
+    assert ir.invrope_take_device_fault() == 0
 
 
 @pytest.mark.parametrize("nh,nope,pe", [(64, 0, 64), (16, 0, 32), (64, 8, 56), (16, 0, 128), (32, 4, 60)])
