@@ -180,7 +180,7 @@ struct PostmixParams {
   int stacked;         // bwd, nh = 64, pe block = one whole chunk: stacked head mix (below)
   const int32_t* pos;  // per-row positions (pos0 is added), or null: row s sits at pos0 + s
   int gs;              // heads per group of the head mix (nh: one [nh, nh] matrix)
-  int m_bulk;          // forward: M is copied into shared memory by one bulk copy at start
+  int m_bulk;          // M is copied into shared memory by one bulk copy at start (if it fits)
   // General tiling (the pe block does not lie inside one 64-channel box): channel
   // tiles [0, n_nope_ct) cover channels [0, nope & ~7) through the clipped maps;
   // tile n_nope_ct + j is pair block j, rotation pairs [32 j, 32 j + 32) of the
@@ -527,6 +527,13 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK, (!BWD || WIDE) && GEN>::k
   const int64_t t_first = BWD ? t_begin : static_cast<int64_t>(blockIdx.x);
   const bool early = BWD ? t_begin < t_end : t_first < p.n_tiles;
 
+  // M's bulk copy lands in the output ring (forward: and the buffers after it,
+  // up to the rotation tables; backward: the ring alone, as X_lo behind it is
+  // zeroed meanwhile). A copy that would not fit is not made, whatever the
+  // host asked: the A build then reads M from L2.
+  const bool m_copy = p.m_bulk != 0 &&
+                      p.nh * p.gs * 4 <= (BWD ? C::kOutBufs * kChunkBytes : C::kOffTabEpi - C::kOffOut);
+
   // ------------------------------------------------------------ setup
   bool sched_mine = false;
   // forward launches with more than two tiles per CTA, backward ones with tail blocks
@@ -564,7 +571,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK, (!BWD || WIDE) && GEN>::k
     ptx::fence_mbar_init();
     // M goes out first, ahead of every tile load (into the output ring, idle
     // until the first tile is mixed); the A build waits on it
-    if (p.m_bulk) {
+    if (m_copy) {
       const uint32_t mbytes = static_cast<uint32_t>(p.nh * p.gs * 4);
       ptx::mbar_arrive_expect_tx(bar_m, mbytes);
       ptx::bulk_load(base + C::kOffOut, p.M, mbytes, bar_m);
@@ -586,7 +593,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK, (!BWD || WIDE) && GEN>::k
     // before anything warp-collective follows
     const char* mb = reinterpret_cast<const char*>(p.M);
     const int mbytes = p.nh * p.gs * 4;
-    if (!p.m_bulk)
+    if (!m_copy)
       for (int o = lane * 128; o < mbytes; o += 32 * 128) ptx::prefetch_l2(mb + o);
     __syncwarp();
   }
@@ -683,7 +690,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK, (!BWD || WIDE) && GEN>::k
       // Ungrouped M with a 16-byte-aligned start: M in shared memory once its
       // bulk copy has landed (the copy left ahead of every tile load);
       // otherwise the entries come from L2.
-      const bool msm = p.m_bulk != 0;
+      const bool msm = m_copy;
       if (msm) wait_bar(bar_m, 0, abort_flag, (kRoleEpilogue << 8) | kBarM);
       const float* Msm = reinterpret_cast<const float*>(gbase + C::kOffOut);  // [nh][nh]
       if constexpr (STK) {
@@ -1784,7 +1791,7 @@ __global__ void __launch_bounds__(KCfg<BWD, WIDE, STK, (!BWD || WIDE) && GEN>::k
   // ------------------------------------------------------------ teardown
   // M's bulk copy must have landed before the CTA leaves (it has, unless the
   // CTA gave up early): bounded wait that ignores the abort flag
-  if (p.m_bulk && threadIdx.x == 0) wait_bar_noabort(bar_m, 0);
+  if (m_copy && threadIdx.x == 0) wait_bar_noabort(bar_m, 0);
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -2236,8 +2243,11 @@ extern "C" int invrope_postmix_bwd_ex(const void* dY, const void* O, const float
     // output ring, idle until the first tile is mixed), when it fits there:
     // the X_lo buffer behind the ring is zeroed while the copy may still be
     // landing. Otherwise (nh = 128) the A build reads M from L2.
-    const int out_ring = (wide ? KCfg<true, true>::kOutBufs
-                               : s.stacked ? KCfg<true, false, true>::kOutBufs : KCfg<true>::kOutBufs) *
+    // (the ring of the exact build launched below)
+    const int out_ring = (wide        ? (s.gen ? KCfg<true, true, false, true>::kOutBufs
+                                               : KCfg<true, true, false, false>::kOutBufs)
+                          : s.stacked ? KCfg<true, false, true>::kOutBufs
+                                      : KCfg<true>::kOutBufs) *
                          kChunkBytes;
     p.m_bulk = (aligned(M, 16) && gs == nh && nh % 2 == 0 && nh * gs * 4 <= out_ring) ? 1 : 0;
     p.n_static = tail.n_static;
